@@ -1,0 +1,135 @@
+/*
+ * ra.h — C ABI of the GB300 (sm_103a) blockwise ring attention library (libra.so).
+ *
+ * What it computes
+ * ----------------
+ * Exact softmax attention  out = softmax(Q K^T / sqrt(d)) V  per (batch, head)
+ * ("Ring Attention with Blockwise Transformers for Near-Infinite Context",
+ * paper review page, §三 核心公式 / 自注意力), evaluated the Ring Attention way:
+ * the sequence is cut into `num_shards` equal contiguous blocks (same page,
+ * 分块注意力), and every query block j combines the key/value blocks in ring
+ * order k = (j - i) mod N, i = 0..N-1 (same page, 环形注意力算法), with the
+ * lazy-softmax running max / numerator / denominator update
+ * ("从论文到代码：深入理解RingAttention的块注意力计算逻辑", §2 数值稳定的注意力计算).
+ * On one GPU the N ring devices are N virtual shards visited inside one
+ * launch; there is no collective.  Masks:
+ *   causal_block_size c > 0:  key j visible to query i iff i / c >= j / c
+ *                             (integer division; code walk-through page §3).
+ *                             Tiles with no visible element are skipped.
+ *   segment_ids (optional):   key j visible to query i iff ids are equal.
+ * The result does not depend on the visit order beyond rounding (paper review
+ * page, 排列不变性), so query_chunk_size / key_chunk_size are validated (the
+ * pages floor-divide the shard by them, code walk-through page §1) but do not
+ * change the result; the kernels use their own 128-row tiles inside each shard.
+ *
+ * Layouts (all row-major, contiguous, device memory)
+ * ------------------------------------------------
+ *   q, k, v, out, dout, dq, dk, dv : [batch, seq, heads, head_dim], element type `dtype`
+ *   lse                            : [batch, heads, seq] float32, natural-log
+ *                                    log-sum-exp of the scaled scores of each query row
+ *                                    (-inf for a row with no visible key; its out row is 0)
+ *   segment_ids                    : [batch, seq] int32, or NULL for no segment mask
+ *
+ * Supported: dtype RA_BF16 with head_dim in {64, 128} (tensor-core path:
+ * TMA-staged tiles, tcgen05 MMAs accumulating in tensor memory), and dtype
+ * RA_F32 with 1 <= head_dim <= 128 (exact fp32 CUDA-core path).
+ * Requirements (else RA_ERR_INVALID_ARG): non-NULL tensor pointers, every
+ * pointer 16-byte aligned, batch, heads >= 1, seq >= 0, num_shards >= 1,
+ * seq % num_shards == 0, (seq / num_shards) % query_chunk_size == 0 and
+ * % key_chunk_size == 0 (chunk sizes >= 1; seq = 0 is an empty problem and
+ * returns RA_OK at once), causal_block_size >= 0, and
+ * batch*seq*heads*head_dim < 2^31.
+ *
+ * Ownership and streams
+ * ---------------------
+ * The caller allocates every buffer.  The library allocates no device memory,
+ * keeps no pointer after a call returns, and enqueues all work on `stream`
+ * (a cudaStream_t; NULL = the legacy default stream).  Calls are asynchronous:
+ * a CUDA launch error is reported at once (RA_ERR_CUDA); a device-side wait
+ * that ran out (RA_ERR_TIMEOUT) is recorded in a device status word and
+ * reported by ra_sync_check.
+ *
+ * Errors
+ * ------
+ * Every function returns an ra_status.  On a non-OK status ra_last_error()
+ * returns a message for the calling thread.  No function aborts the process.
+ */
+#ifndef RA_H_
+#define RA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = 1,  /* bad pointer, shape, alignment or divisibility */
+  RA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement  */
+  RA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed          */
+  RA_ERR_TIMEOUT = 4       /* a bounded device-side wait ran out            */
+} ra_status;
+
+typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
+
+/*
+ * Forward: out, lse <- attention(q, k, v).
+ * One persistent kernel launch for RA_BF16; one launch for RA_F32.
+ */
+ra_status ra_fwd(const void* q, const void* k, const void* v,
+                 const int32_t* segment_ids, int causal_block_size,
+                 int num_shards, int query_chunk_size, int key_chunk_size,
+                 int batch, int seq, int heads, int head_dim, ra_dtype dtype,
+                 void* out, float* lse, void* stream);
+
+/*
+ * Bytes of device scratch that ra_bwd needs for this shape (float32 dQ
+ * accumulator and the per-row Delta = rowsum(dO * out)).  The caller
+ * allocates it; its contents on entry do not matter.
+ */
+size_t ra_bwd_workspace_size(int batch, int seq, int heads, int head_dim, ra_dtype dtype);
+
+/*
+ * Backward: dq, dk, dv <- gradients of sum(dout * out) with respect to q, k, v,
+ * recomputing P = exp(S - lse) from the saved lse (no S x S matrix is stored).
+ * `out` and `lse` are the forward's results for the same inputs.  Same
+ * arguments and rules as ra_fwd; `workspace` must hold
+ * ra_bwd_workspace_size(...) bytes (16-byte aligned).
+ */
+ra_status ra_bwd(const void* q, const void* k, const void* v,
+                 const void* out, const float* lse, const void* dout,
+                 const int32_t* segment_ids, int causal_block_size,
+                 int num_shards, int query_chunk_size, int key_chunk_size,
+                 int batch, int seq, int heads, int head_dim, ra_dtype dtype,
+                 void* dq, void* dk, void* dv,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronize `stream`, then read and clear the device status word that the
+ * kernels set when a bounded wait runs out.  Returns RA_ERR_TIMEOUT (message
+ * names the wait site) if any kernel gave up since the last check,
+ * RA_ERR_CUDA if the stream reports an error, else RA_OK.
+ */
+ra_status ra_sync_check(void* stream);
+
+/* Message for the last non-OK status returned to the calling thread ("" if none). */
+const char* ra_last_error(void);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t ra_kernel_launches(void);
+
+/*
+ * Diagnostic: launch one tiny kernel that waits on a barrier nothing will
+ * ever complete, bounded by `limit_ns` nanoseconds (<= 1e9).  The kernel gives
+ * up, records a timeout in the device status word and returns, leaving the
+ * context usable; ra_sync_check then reports RA_ERR_TIMEOUT.
+ */
+ra_status ra_selftest_timeout(int64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H_ */

@@ -1,0 +1,679 @@
+// attn_fwd_sm103.cu — bf16 forward of blockwise ring attention on sm_103a.
+//
+// What it computes: per (batch, head), out = softmax(Q K^T / sqrt(d)) V and the
+// natural-log lse of each row ("Ring Attention with Blockwise Transformers for
+// Near-Infinite Context", paper review page, §三 核心公式), with the sequence
+// split into N contiguous virtual shards and each query shard j visiting the
+// KV shards in ring order k = (j - i) mod N (same page, 环形注意力算法).  The
+// running max / numerator / denominator update is the lazy softmax of the code
+// walk-through page ("从论文到代码：深入理解RingAttention的块注意力计算逻辑",
+// §2 数值稳定的注意力计算); tiles with no visible element are skipped (§3,
+// below_or_on_diag), and segment ids mask across documents.
+//
+// How (one persistent CTA per SM, 10 warps):
+//   warps 0-3  softmax warpgroup for Q tile 0 (TMEM lanes 0-127, one row per thread)
+//   warps 4-7  softmax warpgroup for Q tile 1
+//   warp 8     producer: walks the ring schedule, classifies each 128-key tile
+//              (skip / full / needs a mask), publishes a record per visible
+//              tile and TMA-loads K and V into a smem ring (128B swizzle)
+//   warp 9     MMA issuer: S_w = Q_w K^T (SS, fp32 in TMEM), then
+//              O_w += P_w V with P_w read from TMEM (TS), ping-ponging the two
+//              Q tiles so the tensor pipe runs one tile's MMAs while the other
+//              tile's softmax runs.
+// Tensor memory (512 columns): S0 | S1 | O0 | O1.  P_w is written as packed
+// bf16 pairs over the first 64 columns of S_w.
+// The running max is only moved (and O, l rescaled) when a row's tile max
+// exceeds it by more than 2^8; in exact arithmetic the result is unchanged
+// (numerator and denominator carry the same factor), and the exponentials
+// stay <= 256.  Every mbarrier wait is bounded (see sm103.cuh).
+#include <cmath>
+#include <cstdint>
+#include <cudaTypedefs.h>
+
+#include "ra_internal.h"
+#include "sm103.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kBM = 128;  // rows per Q tile
+constexpr int kBN = 128;  // keys per KV tile
+constexpr int kNInfo = 8; // schedule-record ring depth
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+enum : int { kRecTile = 0, kRecUnitEnd = 1, kRecStop = 2 };
+enum : int { kSkip0 = 1, kSkip1 = 2, kMask0 = 4, kMask1 = 8 };
+
+struct __align__(16) Rec {
+  int kind;
+  int flags;
+  int kstart;   // first key (global sequence index) of the tile
+  int kvalid;   // keys of the tile that lie inside the shard (1..128)
+  int b, h;
+  int q0;       // first row of Q tile 0 (global); tile 1 starts at q0 + 128
+  int qvalid0, qvalid1;  // rows of each Q tile inside the shard (0 = tile absent)
+  int pad[3];
+};
+
+template <int D>
+struct Cfg {
+  static constexpr int KST = (D == 64) ? 4 : 2;          // K/V ring stages
+  static constexpr uint32_t QT = kBM * D * 2;            // bytes of one Q tile
+  static constexpr uint32_t KVT = kBN * D * 2;           // bytes of one K or V tile
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * QT;
+  static constexpr uint32_t OFF_V = OFF_K + KST * KVT;
+  static constexpr uint32_t OFF_REC = OFF_V + KST * KVT;
+  static constexpr uint32_t OFF_BAR = OFF_REC + kNInfo * sizeof(Rec);
+  // barriers: qfull, qempty, kfull[KST], kempty[KST], vfull[KST], vempty[KST],
+  //           infofull[8], infoempty[8], sfull[2], pready[2], odone[2], ofree[2]
+  static constexpr int NBAR = 2 + 4 * KST + 2 * kNInfo + 8;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
+  static constexpr uint32_t TCOL_O = 256;                 // O0 at 256, O1 at 256 + D
+};
+
+struct Bars {
+  uint32_t base;
+  int kst;
+  __device__ uint32_t qfull() const { return base; }
+  __device__ uint32_t qempty() const { return base + 8; }
+  __device__ uint32_t kfull(int s) const { return base + 16 + 8 * s; }
+  __device__ uint32_t kempty(int s) const { return base + 16 + 8 * (kst + s); }
+  __device__ uint32_t vfull(int s) const { return base + 16 + 8 * (2 * kst + s); }
+  __device__ uint32_t vempty(int s) const { return base + 16 + 8 * (3 * kst + s); }
+  __device__ uint32_t infofull(int i) const { return base + 16 + 8 * (4 * kst + i); }
+  __device__ uint32_t infoempty(int i) const { return base + 16 + 8 * (4 * kst + kNInfo + i); }
+  __device__ uint32_t sfull(int w) const { return base + 16 + 8 * (4 * kst + 2 * kNInfo + w); }
+  __device__ uint32_t pready(int w) const { return base + 16 + 8 * (4 * kst + 2 * kNInfo + 2 + w); }
+  __device__ uint32_t odone(int w) const { return base + 16 + 8 * (4 * kst + 2 * kNInfo + 4 + w); }
+  __device__ uint32_t ofree(int w) const { return base + 16 + 8 * (4 * kst + 2 * kNInfo + 6 + w); }
+};
+
+struct FwdParams {
+  Problem p;
+  __nv_bfloat16* out;
+  float* lse;
+  int* status;
+  uint64_t limit_ns;
+  int tiles_per_shard;  // ceil(Ssh / 128)
+  int pairs_per_shard;  // ceil(tiles_per_shard / 2)
+  int num_units;        // B * H * N * pairs_per_shard
+  float scale_log2;     // log2(e) / sqrt(D)
+};
+
+__device__ __forceinline__ int floordiv_pos(int a, int c) { return a / c; }  // a >= 0
+
+// Unit u -> (b, h, query shard j, pair index).  Units are ordered by
+// decreasing global query position (longest causal work first), heads and
+// batches interleaved; CTA c takes units c, c + G, c + 2G, ...
+__device__ __forceinline__ void unit_coords(const FwdParams& P, int u, int& b, int& h, int& j, int& pr) {
+  const int BH = P.p.B * P.p.H;
+  const int rank = u / BH;
+  const int bh = u % BH;
+  const int g = P.p.N * P.pairs_per_shard - 1 - rank;
+  j = g / P.pairs_per_shard;
+  pr = g % P.pairs_per_shard;
+  b = bh / P.p.H;
+  h = bh % P.p.H;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_bf16_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                    const __grid_constant__ CUtensorMap mv, const FwdParams P) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  const uint32_t sbase = smem_u32(sm);
+  Rec* recs = reinterpret_cast<Rec*>(sm + C::OFF_REC);
+  Bars bars{sbase + C::OFF_BAR, C::KST};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bars.qfull(), 1);
+    mbar_init(bars.qempty(), 1);
+    for (int s = 0; s < C::KST; ++s) {
+      mbar_init(bars.kfull(s), 1);
+      mbar_init(bars.kempty(s), 1);
+      mbar_init(bars.vfull(s), 1);
+      mbar_init(bars.vempty(s), 1);
+    }
+    for (int i = 0; i < kNInfo; ++i) {
+      mbar_init(bars.infofull(i), 1);
+      mbar_init(bars.infoempty(i), 1 + 256);  // MMA thread + every softmax thread
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(bars.sfull(w), 1);
+      mbar_init(bars.pready(w), 128);
+      mbar_init(bars.odone(w), 1);
+      mbar_init(bars.ofree(w), 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  WaitCtl ctl{P.status, abort_flag, P.limit_ns};
+  const Problem& pb = P.p;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------------
+    // Producer: ring schedule + TMA
+    // ------------------------------------------------------------------
+    if (lane == 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+    }
+    int rec_n = 0, tile_n = 0, unit_n = 0, q_loads = 0;
+    bool alive = true;
+    const int c = pb.causal;
+    // publish a record (lane 0 only); returns false on abort
+    auto publish = [&](const Rec& r) -> bool {
+      const int slot = rec_n % kNInfo;
+      if (!mbar_wait(bars.infoempty(slot), ((rec_n / kNInfo) & 1) ^ 1, ctl, 10)) return false;
+      recs[slot] = r;
+      mbar_arrive(bars.infofull(slot));
+      ++rec_n;
+      return true;
+    };
+    for (int u = blockIdx.x; u < P.num_units && alive; u += gridDim.x) {
+      int b, h, j, pr;
+      unit_coords(P, u, b, h, j, pr);
+      const int shard0 = j * pb.Ssh;
+      const int q0 = shard0 + pr * 2 * kBM;
+      const int qv0 = max(0, min(kBM, shard0 + pb.Ssh - q0));
+      const int qv1 = max(0, min(kBM, shard0 + pb.Ssh - (q0 + kBM)));
+      // segment range of each Q tile
+      int qmin[2] = {0, 0}, qmax[2] = {0, 0};
+      if (pb.seg) {
+        for (int w = 0; w < 2; ++w) {
+          const int nv = w == 0 ? qv0 : qv1;
+          int mn = INT_MAX, mx = INT_MIN;
+          for (int r = lane; r < nv; r += 32) {
+            const int sv = __ldg(pb.seg + (size_t)b * pb.S + q0 + w * kBM + r);
+            mn = min(mn, sv);
+            mx = max(mx, sv);
+          }
+          for (int o = 16; o > 0; o >>= 1) {
+            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          }
+          qmin[w] = mn;
+          qmax[w] = mx;
+        }
+      }
+      // Q tiles (wait until the previous unit's S MMAs have finished with Q smem)
+      if (lane == 0) {
+        alive = mbar_wait(bars.qempty(), (unit_n & 1) ^ 1, ctl, 11);
+        if (alive) {
+          ++q_loads;
+          mbar_arrive_expect_tx(bars.qfull(), 2 * C::QT);
+          for (int w = 0; w < 2; ++w)
+            for (int cb = 0; cb < D / 64; ++cb)
+              tma_load_4d(sbase + C::OFF_Q + w * C::QT + cb * 16384, &mq, bars.qfull(), cb * 64, h,
+                          q0 + w * kBM, b);
+        }
+      }
+      alive = __shfl_sync(0xffffffffu, alive, 0);
+      const int qlast0 = q0 + max(qv0, 1) - 1;
+      const int qlast1 = q0 + kBM + max(qv1, 1) - 1;
+      const int qlast = qv1 > 0 ? qlast1 : qlast0;
+      for (int i = 0; i < pb.N && alive; ++i) {
+        const int ks = ((j - i) % pb.N + pb.N) % pb.N;  // ring order
+        const int kbeg = ks * pb.Ssh, kend = kbeg + pb.Ssh;
+        if (c > 0 && floordiv_pos(qlast, c) < floordiv_pos(kbeg, c)) continue;  // whole shard in the future
+        for (int t0 = 0; t0 < P.tiles_per_shard && alive; t0 += 32) {
+          // tile segment ranges, one tile per lane
+          int kmn = 0, kmx = 0;
+          const int my_t = t0 + lane;
+          if (pb.seg && my_t < P.tiles_per_shard) {
+            const int ka = kbeg + my_t * kBN;
+            const int kb = min(kend, ka + kBN);
+            bool needed = !(c > 0 && floordiv_pos(qlast, c) < floordiv_pos(ka, c));
+            int mn = INT_MAX, mx = INT_MIN;
+            if (needed) {
+              const int* sp = pb.seg + (size_t)b * pb.S;
+              for (int x = ka; x < kb; ++x) {
+                const int sv = __ldg(sp + x);
+                mn = min(mn, sv);
+                mx = max(mx, sv);
+              }
+            }
+            kmn = mn;
+            kmx = mx;
+          }
+          const int tend = min(32, P.tiles_per_shard - t0);
+          for (int tt = 0; tt < tend && alive; ++tt) {
+            const int t = t0 + tt;
+            const int ka = kbeg + t * kBN;
+            const int kvalid = min(kBN, kend - ka);
+            const int kb = ka + kvalid - 1;
+            const int tmn = __shfl_sync(0xffffffffu, kmn, tt);
+            const int tmx = __shfl_sync(0xffffffffu, kmx, tt);
+            int flags = 0;
+            for (int w = 0; w < 2; ++w) {
+              const int qv = w == 0 ? qv0 : qv1;
+              const int qa = q0 + w * kBM, ql = qa + qv - 1;
+              bool skip = qv == 0, full = true;
+              if (!skip && c > 0) {
+                if (floordiv_pos(ql, c) < floordiv_pos(ka, c)) skip = true;
+                else if (!(floordiv_pos(qa, c) >= floordiv_pos(kb, c))) full = false;
+              }
+              if (!skip && pb.seg) {
+                if (tmx < qmin[w] || tmn > qmax[w]) skip = true;
+                else if (!(qmin[w] == qmax[w] && tmn == qmax[w] && tmx == qmax[w])) full = false;
+              }
+              if (kvalid < kBN) full = false;
+              if (skip) flags |= (w == 0 ? kSkip0 : kSkip1);
+              else if (!full) flags |= (w == 0 ? kMask0 : kMask1);
+            }
+            if ((flags & (kSkip0 | kSkip1)) == (kSkip0 | kSkip1)) continue;
+            if (lane == 0) {
+              Rec r;
+              r.kind = kRecTile;
+              r.flags = flags;
+              r.kstart = ka;
+              r.kvalid = kvalid;
+              r.b = b;
+              r.h = h;
+              r.q0 = q0;
+              r.qvalid0 = qv0;
+              r.qvalid1 = qv1;
+              alive = publish(r);
+              const int s = tile_n % C::KST;
+              const uint32_t par = ((tile_n / C::KST) & 1) ^ 1;
+              if (alive) alive = mbar_wait(bars.kempty(s), par, ctl, 12);
+              if (alive) {
+                mbar_arrive_expect_tx(bars.kfull(s), C::KVT);
+                for (int cb = 0; cb < D / 64; ++cb)
+                  tma_load_4d(sbase + C::OFF_K + s * C::KVT + cb * 16384, &mk, bars.kfull(s), cb * 64, h, ka, b);
+              }
+              if (alive) alive = mbar_wait(bars.vempty(s), par, ctl, 13);
+              if (alive) {
+                mbar_arrive_expect_tx(bars.vfull(s), C::KVT);
+                for (int cb = 0; cb < D / 64; ++cb)
+                  tma_load_4d(sbase + C::OFF_V + s * C::KVT + cb * 16384, &mv, bars.vfull(s), cb * 64, h, ka, b);
+              }
+              ++tile_n;
+            }
+            alive = __shfl_sync(0xffffffffu, alive, 0);
+          }
+        }
+      }
+      if (lane == 0 && alive) {
+        Rec r;
+        r.kind = kRecUnitEnd;
+        r.flags = 0;
+        r.kstart = 0;
+        r.kvalid = 0;
+        r.b = b;
+        r.h = h;
+        r.q0 = q0;
+        r.qvalid0 = qv0;
+        r.qvalid1 = qv1;
+        alive = publish(r);
+      }
+      alive = __shfl_sync(0xffffffffu, alive, 0);
+      ++unit_n;
+    }
+    if (lane == 0 && alive) {
+      Rec r;
+      r.kind = kRecStop;
+      publish(r);
+    }
+    // Let every issued copy land before the CTA can exit (bounded, ignores abort).
+    if (lane == 0) {
+      for (int s = 0; s < C::KST; ++s) {
+        if (tile_n <= s) continue;
+        const int last = s + ((tile_n - 1 - s) / C::KST) * C::KST;  // last tile that used stage s
+        const uint32_t par = (last / C::KST) & 1;
+        mbar_drain(bars.kfull(s), par, ctl, 14);
+        mbar_drain(bars.vfull(s), par, ctl, 15);
+      }
+      if (q_loads > 0) mbar_drain(bars.qfull(), (q_loads - 1) & 1, ctl, 16);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------
+    // MMA issuer (lane 0)
+    // ------------------------------------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
+      constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 0, 1);
+      int rec_n = 0, tile_n = 0, unit_n = 0;
+      uint32_t ofree_ph[2] = {1, 1}, pready_ph[2] = {0, 0};
+      bool alive = true;
+      auto take = [&](Rec& r) -> bool {
+        const int slot = rec_n % kNInfo;
+        if (!mbar_wait(bars.infofull(slot), (rec_n / kNInfo) & 1, ctl, 20)) return false;
+        r = recs[slot];
+        return true;
+      };
+      auto release = [&](int n) { mbar_arrive(bars.infoempty(n % kNInfo)); };
+      auto issue_S = [&](const Rec& r, int stage) -> bool {
+        if (!mbar_wait(bars.kfull(stage), (tile_n / C::KST) & 1, ctl, 21)) return false;
+        tc_fence_after();
+        for (int w = 0; w < 2; ++w) {
+          if (r.flags & (w == 0 ? kSkip0 : kSkip1)) continue;
+          const uint32_t qa = sbase + C::OFF_Q + w * C::QT;
+          const uint32_t ka = sbase + C::OFF_K + stage * C::KVT;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(tbase + w * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS,
+                   kk > 0);
+          }
+          mma_commit(bars.sfull(w));
+        }
+        mma_commit(bars.kempty(stage));
+        return true;
+      };
+      Rec rec, nxt;
+      alive = take(rec);
+      while (alive && rec.kind != kRecStop) {
+        // rec is the first tile of a unit
+        alive = mbar_wait(bars.qfull(), unit_n & 1, ctl, 22);
+        if (alive && rec.kind == kRecUnitEnd) {  // a unit without visible tiles
+          mma_commit(bars.qempty());
+          release(rec_n);
+          ++rec_n;
+          ++unit_n;
+          alive = take(rec);
+          continue;
+        }
+        int stage = tile_n % C::KST;
+        if (alive) alive = issue_S(rec, stage);
+        bool first[2] = {true, true};
+        bool any_pv[2] = {false, false};
+        while (alive) {
+          ++rec_n;
+          alive = take(nxt);
+          if (!alive) break;
+          // PV for rec, interleaved with S for nxt
+          if (!mbar_wait(bars.vfull(stage), (tile_n / C::KST) & 1, ctl, 23)) { alive = false; break; }
+          const int nstage = (tile_n + 1) % C::KST;
+          bool nxt_k_ready = false;
+          for (int w = 0; w < 2 && alive; ++w) {
+            if (!(rec.flags & (w == 0 ? kSkip0 : kSkip1))) {
+              if (first[w]) {
+                if (!mbar_wait(bars.ofree(w), ofree_ph[w], ctl, 24)) { alive = false; break; }
+                ofree_ph[w] ^= 1;
+              }
+              if (!mbar_wait(bars.pready(w), pready_ph[w], ctl, 25)) { alive = false; break; }
+              pready_ph[w] ^= 1;
+              tc_fence_after();
+              const uint32_t va = sbase + C::OFF_V + stage * C::KVT;
+#pragma unroll
+              for (int kk = 0; kk < kBN / 16; ++kk)
+                mma_ts(tbase + C::TCOL_O + w * D, tbase + w * 128 + kk * 8,
+                       sdesc_sw128(va + kk * 2048, 16384, 1024), idO, first[w] ? (kk > 0) : 1);
+              first[w] = false;
+              any_pv[w] = true;
+            }
+            if (nxt.kind == kRecTile && !(nxt.flags & (w == 0 ? kSkip0 : kSkip1))) {
+              if (!nxt_k_ready) {
+                if (!mbar_wait(bars.kfull(nstage), ((tile_n + 1) / C::KST) & 1, ctl, 26)) { alive = false; break; }
+                tc_fence_after();
+                nxt_k_ready = true;
+              }
+              const uint32_t qa = sbase + C::OFF_Q + w * C::QT;
+              const uint32_t ka = sbase + C::OFF_K + nstage * C::KVT;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                mma_ss(tbase + w * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS,
+                       kk > 0);
+              }
+              mma_commit(bars.sfull(w));
+            }
+          }
+          if (!alive) break;
+          mma_commit(bars.vempty(stage));
+          if (nxt.kind == kRecTile) mma_commit(bars.kempty(nstage));
+          release(rec_n - 1);
+          ++tile_n;
+          stage = nstage;
+          if (nxt.kind != kRecTile) {  // unit end
+            for (int w = 0; w < 2; ++w)
+              if (any_pv[w]) mma_commit(bars.odone(w));
+            mma_commit(bars.qempty());
+            release(rec_n);
+            ++rec_n;
+            ++unit_n;
+            break;
+          }
+          rec = nxt;
+        }
+        if (!alive) break;
+        alive = take(rec);
+      }
+      if (alive && rec.kind == kRecStop) release(rec_n);
+      // Drain: wait for every MMA issued by this thread before TMEM is freed.
+      mma_commit(bars.qempty());
+      mbar_drain(bars.qempty(), (unit_n & 1), ctl, 27);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------
+    // Softmax warpgroups: w = Q tile, one row per thread
+    // ------------------------------------------------------------------
+    const int w = warp >> 2;
+    const int rl = (warp & 3) * 32 + lane;              // row within the tile
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tbase + lane_base + w * 128;
+    const uint32_t tO = tbase + lane_base + C::TCOL_O + w * D;
+    const float sl2 = P.scale_log2;
+    float m_use = -INFINITY, l = 0.f;
+    int processed = 0;
+    uint32_t sfull_ph = 0, odone_ph = 0;
+    int rec_n = 0;
+    bool alive = true;
+    while (alive) {
+      const int slot = rec_n % kNInfo;
+      alive = mbar_wait(bars.infofull(slot), (rec_n / kNInfo) & 1, ctl, 30);
+      alive = __all_sync(0xffffffffu, alive);
+      if (!alive) break;
+      const Rec r = recs[slot];
+      if (r.kind == kRecStop) {
+        mbar_arrive(bars.infoempty(slot));
+        break;
+      }
+      const int qrow = r.q0 + w * kBM + rl;
+      if (r.kind == kRecTile && !(r.flags & (w == 0 ? kSkip0 : kSkip1))) {
+        alive = mbar_wait(bars.sfull(w), sfull_ph, ctl, 31);
+        alive = __all_sync(0xffffffffu, alive);
+        if (!alive) break;
+        sfull_ph ^= 1;
+        tc_fence_after();
+        uint32_t sr[128];
+#pragma unroll
+        for (int cq = 0; cq < 4; ++cq) tmem_ld32(tS + cq * 32, sr + cq * 32);
+#pragma unroll
+        for (int cq = 0; cq < 4; ++cq) tmem_ld_wait(sr + cq * 32);
+        if (r.flags & (w == 0 ? kMask0 : kMask1)) {
+          const int cb = pb.causal;
+          const int qblk = cb > 0 ? qrow / cb : 0;
+          const int qseg = pb.seg ? __ldg(pb.seg + (size_t)r.b * pb.S + min(qrow, pb.S - 1)) : 0;
+          const int* kseg = pb.seg ? pb.seg + (size_t)r.b * pb.S : nullptr;
+#pragma unroll
+          for (int x = 0; x < 128; ++x) {
+            const int key = r.kstart + x;
+            bool vis = x < r.kvalid;
+            if (cb > 0) vis = vis && (qblk >= key / cb);
+            if (kseg) vis = vis && (__ldg(kseg + min(key, pb.S - 1)) == qseg);
+            if (!vis) sr[x] = __float_as_uint(-INFINITY);
+          }
+        }
+        float mx = __uint_as_float(sr[0]);
+#pragma unroll
+        for (int x = 1; x < 128; ++x) mx = fmaxf(mx, __uint_as_float(sr[x]));
+        const float m_tile = mx * sl2;
+        float corr = 1.f;
+        bool resc = false;
+        if (m_tile > m_use + kRescaleThreshold) {
+          if (m_use != -INFINITY) {
+            corr = ex2_approx(m_use - m_tile);
+            resc = true;
+          }
+          m_use = m_tile;
+        }
+        const float mb = (m_use == -INFINITY) ? 0.f : m_use;
+        float rs = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int x = 0; x < 64; ++x) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * x]), sl2, -mb));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * x + 1]), sl2, -mb));
+          rs += p0 + p1;
+          pk[x] = pack_bf16x2(p0, p1);
+        }
+        l = l * corr + rs;
+        tmem_st32(tS, pk);
+        tmem_st32(tS + 32, pk + 32);
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int cq = 0; cq < D / 32; ++cq) {
+            uint32_t o[32];
+            tmem_ld32(tO + cq * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * corr);
+            tmem_st32(tO + cq * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bars.pready(w));
+        ++processed;
+      } else if (r.kind == kRecUnitEnd) {
+        if (processed > 0) {
+          alive = mbar_wait(bars.odone(w), odone_ph, ctl, 32);
+          alive = __all_sync(0xffffffffu, alive);
+          if (!alive) break;
+          odone_ph ^= 1;
+          tc_fence_after();
+          const int qv = w == 0 ? r.qvalid0 : r.qvalid1;
+          const bool store = rl < qv;
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          __nv_bfloat16* orow = P.out + (((size_t)r.b * pb.S + qrow) * pb.H + r.h) * D;
+#pragma unroll
+          for (int cq = 0; cq < D / 32; ++cq) {
+            uint32_t o[32];
+            tmem_ld32(tO + cq * 32, o);
+            tmem_ld_wait(o);
+            if (store) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + cq * 32);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                uint4 val;
+                val.x = pack_bf16x2(__uint_as_float(o[v4 * 8 + 0]) * inv, __uint_as_float(o[v4 * 8 + 1]) * inv);
+                val.y = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2]) * inv, __uint_as_float(o[v4 * 8 + 3]) * inv);
+                val.z = pack_bf16x2(__uint_as_float(o[v4 * 8 + 4]) * inv, __uint_as_float(o[v4 * 8 + 5]) * inv);
+                val.w = pack_bf16x2(__uint_as_float(o[v4 * 8 + 6]) * inv, __uint_as_float(o[v4 * 8 + 7]) * inv);
+                dst[v4] = val;
+              }
+            }
+          }
+          if (store)
+            P.lse[((size_t)r.b * pb.H + r.h) * pb.S + qrow] =
+                l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          tc_fence_before();
+          mbar_arrive(bars.ofree(w));
+        }
+        m_use = -INFINITY;
+        l = 0.f;
+        processed = 0;
+      }
+      mbar_arrive(bars.infoempty(slot));
+      ++rec_n;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tbase, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+  }
+  return fn;
+}
+
+}  // namespace
+
+// [B, S, H, D] bf16 tensor map with a 64-element x 128-row box, 128B swizzle.
+bool make_tile_map(CUtensorMap* m, const void* ptr, const Problem& p, int rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)p.D, (cuuint64_t)p.H, (cuuint64_t)p.S, (cuuint64_t)p.B};
+  cuuint64_t strides[3] = {(cuuint64_t)p.D * 2, (cuuint64_t)p.H * p.D * 2, (cuuint64_t)p.S * p.H * p.D * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
+  using Cf = Cfg<D>;
+  const Problem& p = a.p;
+  CUtensorMap mq, mk, mv;
+  if (!make_tile_map(&mq, a.q, p, kBM) || !make_tile_map(&mk, a.k, p, kBN) || !make_tile_map(&mv, a.v, p, kBN)) {
+    *why = "cuTensorMapEncodeTiled failed (driver entry point unavailable or tensor rejected)";
+    return cudaSuccess;
+  }
+  FwdParams P;
+  P.p = p;
+  P.out = (__nv_bfloat16*)a.out;
+  P.lse = a.lse;
+  P.status = c.status;
+  P.limit_ns = c.limit_ns;
+  P.tiles_per_shard = (p.Ssh + kBN - 1) / kBN;
+  P.pairs_per_shard = (P.tiles_per_shard + 1) / 2;
+  P.num_units = p.B * p.H * p.N * P.pairs_per_shard;
+  P.scale_log2 = (float)(1.4426950408889634 / sqrt((double)p.D));
+  static bool attr_set[256][2];
+  const int di = D == 64 ? 0 : 1;
+  if (!attr_set[c.device][di]) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Cf::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[c.device][di] = true;
+  }
+  const int grid = std::min(c.num_sms, P.num_units);
+  fwd_bf16_kernel<D><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, P);
+  *launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_bf16(const FwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
+  if (a.p.D == 64) return launch_fwd_bf16_d<64>(a, c, launches, why);
+  if (a.p.D == 128) return launch_fwd_bf16_d<128>(a, c, launches, why);
+  *why = "bf16 head_dim must be 64 or 128";
+  return cudaSuccess;
+}
+
+}  // namespace ra

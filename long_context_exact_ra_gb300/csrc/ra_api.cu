@@ -1,0 +1,240 @@
+// ra_api.cu — the C ABI (include/ra.h): argument validation, dispatch to the
+// kernel launchers, the device status word and per-thread error messages.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/ra.h"
+#include "ra_internal.h"
+
+#define RA_API extern "C" __attribute__((visibility("default")))
+
+namespace ra {
+
+__device__ int g_status;  // kernels record a timed-out wait here (one word per device)
+
+namespace {
+
+thread_local char t_msg[512] = "";
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_mu;
+int* g_status_ptr[256];
+bool g_status_init[256];
+
+ra_status fail(ra_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof(t_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+ra_status ok() {
+  t_msg[0] = 0;
+  return RA_OK;
+}
+
+uint64_t limit_ns_from_env() {
+  const char* e = getenv("RA_WAIT_LIMIT_NS");
+  if (e && *e) {
+    long long v = atoll(e);
+    if (v > 0 && v <= 10000000000LL) return (uint64_t)v;
+  }
+  return 2000000000ull;  // 2 s: every legitimate wait is microseconds
+}
+
+ra_status make_ctx(void* stream, Ctx* c) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 256) return fail(RA_ERR_CUDA, "device ordinal %d out of range", dev);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_init[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_status);
+      if (e != cudaSuccess)
+        return fail(RA_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+      e = cudaMemset(p, 0, sizeof(int));
+      if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaMemset(status): %s", cudaGetErrorString(e));
+      g_status_ptr[dev] = (int*)p;
+      g_status_init[dev] = true;
+    }
+    c->status = g_status_ptr[dev];
+  }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+  c->device = dev;
+  c->num_sms = sms;
+  c->limit_ns = limit_ns_from_env();
+  c->stream = (cudaStream_t)stream;
+  return RA_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+ra_status validate(const void* const* ptrs, const char* const* names, int nptr,
+                   const int32_t* seg, int causal_block_size, int num_shards, int qc, int kc,
+                   int B, int S, int H, int D, ra_dtype dtype, Problem* p) {
+  if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (B < 1 || H < 1 || S < 0 || D < 1)
+    return fail(RA_ERR_INVALID_ARG, "bad shape B=%d S=%d H=%d D=%d", B, S, H, D);
+  if ((long long)B * S * H * D >= (1LL << 31))
+    return fail(RA_ERR_INVALID_ARG, "B*S*H*D = %lld must be < 2^31", (long long)B * S * H * D);
+  if (num_shards < 1) return fail(RA_ERR_INVALID_ARG, "num_shards=%d must be >= 1", num_shards);
+  if (S % num_shards != 0)
+    return fail(RA_ERR_INVALID_ARG, "seq=%d not divisible by num_shards=%d", S, num_shards);
+  if (qc < 1 || kc < 1)
+    return fail(RA_ERR_INVALID_ARG, "chunk sizes must be >= 1 (query %d, key %d)", qc, kc);
+  const int Ssh = S / num_shards;
+  if (Ssh % qc != 0 || Ssh % kc != 0)
+    return fail(RA_ERR_INVALID_ARG, "shard length %d not divisible by query_chunk_size=%d / key_chunk_size=%d",
+                Ssh, qc, kc);
+  if (causal_block_size < 0)
+    return fail(RA_ERR_INVALID_ARG, "causal_block_size=%d must be >= 0", causal_block_size);
+  for (int i = 0; i < nptr; ++i) {
+    if (ptrs[i] == nullptr) return fail(RA_ERR_INVALID_ARG, "%s is NULL", names[i]);
+    if (!aligned16(ptrs[i])) return fail(RA_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+  }
+  if (seg != nullptr && !aligned16(seg)) return fail(RA_ERR_INVALID_ARG, "segment_ids is not 16-byte aligned");
+  if (dtype == RA_BF16 && D != 64 && D != 128)
+    return fail(RA_ERR_UNSUPPORTED, "bf16 path supports head_dim 64 and 128, got %d", D);
+  if (dtype == RA_F32 && D > 128) return fail(RA_ERR_UNSUPPORTED, "fp32 path supports head_dim <= 128, got %d", D);
+  p->B = B;
+  p->S = S;
+  p->H = H;
+  p->D = D;
+  p->N = num_shards;
+  p->Ssh = Ssh;
+  p->causal = causal_block_size;
+  p->seg = seg;
+  return RA_OK;
+}
+
+}  // namespace
+}  // namespace ra
+
+using namespace ra;
+
+RA_API ra_status ra_fwd(const void* q, const void* k, const void* v, const int32_t* segment_ids,
+                        int causal_block_size, int num_shards, int query_chunk_size, int key_chunk_size,
+                        int batch, int seq, int heads, int head_dim, ra_dtype dtype, void* out, float* lse,
+                        void* stream) {
+  const void* ptrs[] = {q, k, v, out, lse};
+  const char* names[] = {"q", "k", "v", "out", "lse"};
+  FwdArgs a;
+  ra_status s = validate(ptrs, names, 5, segment_ids, causal_block_size, num_shards, query_chunk_size,
+                         key_chunk_size, batch, seq, heads, head_dim, dtype, &a.p);
+  if (s != RA_OK) return s;
+  if (seq == 0) return ok();
+  Ctx c;
+  if ((s = make_ctx(stream, &c)) != RA_OK) return s;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  uint64_t n = 0;
+  cudaError_t e;
+  const char* why = nullptr;
+  if (dtype == RA_F32) {
+    e = launch_fwd_f32(a, c, &n);
+  } else {
+    e = launch_fwd_bf16(a, c, &n, &why);
+  }
+  g_launches += n;
+  if (why) return fail(RA_ERR_UNSUPPORTED, "%s", why);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+RA_API size_t ra_bwd_workspace_size(int batch, int seq, int heads, int head_dim, ra_dtype dtype) {
+  if (batch < 1 || seq < 0 || heads < 1 || head_dim < 1) return 0;
+  if (dtype == RA_F32) {
+    return (((size_t)batch * heads * seq * sizeof(float)) + 255) & ~(size_t)255;  // Delta only
+  }
+  return bwd_workspace_bytes(batch, seq, heads, head_dim);
+}
+
+RA_API ra_status ra_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                        const void* dout, const int32_t* segment_ids, int causal_block_size, int num_shards,
+                        int query_chunk_size, int key_chunk_size, int batch, int seq, int heads, int head_dim,
+                        ra_dtype dtype, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  const void* ptrs[] = {q, k, v, out, lse, dout, dq, dk, dv, workspace};
+  const char* names[] = {"q", "k", "v", "out", "lse", "dout", "dq", "dk", "dv", "workspace"};
+  BwdArgs a;
+  ra_status s = validate(ptrs, names, 10, segment_ids, causal_block_size, num_shards, query_chunk_size,
+                         key_chunk_size, batch, seq, heads, head_dim, dtype, &a.p);
+  if (s != RA_OK) return s;
+  const size_t need = ra_bwd_workspace_size(batch, seq, heads, head_dim, dtype);
+  if (workspace_bytes < need)
+    return fail(RA_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", workspace_bytes, need);
+  if (seq == 0) return ok();
+  Ctx c;
+  if ((s = make_ctx(stream, &c)) != RA_OK) return s;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  uint64_t n = 0;
+  cudaError_t e;
+  const char* why = nullptr;
+  if (dtype == RA_F32) {
+    a.dq_accum = nullptr;
+    a.delta = (float*)workspace;
+    e = launch_bwd_f32(a, c, &n);
+  } else {
+    a.dq_accum = (float*)workspace;
+    a.delta = (float*)((char*)workspace + bwd_delta_offset(batch, seq, heads, head_dim));
+    e = launch_bwd_bf16(a, c, &n, &why);
+  }
+  g_launches += n;
+  if (why) return fail(RA_ERR_UNSUPPORTED, "%s", why);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+RA_API ra_status ra_sync_check(void* stream) {
+  Ctx c;
+  ra_status s = make_ctx(stream, &c);
+  if (s != RA_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(c.stream);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  int word = 0;
+  e = cudaMemcpy(&word, c.status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "reading status word: %s", cudaGetErrorString(e));
+  if (word != 0) {
+    int zero = 0;
+    cudaMemcpy(c.status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    return fail(RA_ERR_TIMEOUT, "a device-side wait ran out (site %d)", word & 0xFFFF);
+  }
+  return ok();
+}
+
+RA_API const char* ra_last_error(void) { return t_msg; }
+
+RA_API uint64_t ra_kernel_launches(void) { return g_launches.load(); }
+
+RA_API ra_status ra_selftest_timeout(int64_t limit_ns, void* stream) {
+  if (limit_ns < 1 || limit_ns > 1000000000LL)
+    return fail(RA_ERR_INVALID_ARG, "limit_ns=%lld must be in [1, 1e9]", (long long)limit_ns);
+  Ctx c;
+  ra_status s = make_ctx(stream, &c);
+  if (s != RA_OK) return s;
+  c.limit_ns = (uint64_t)limit_ns;
+  uint64_t n = 0;
+  cudaError_t e = launch_selftest_timeout(c, &n);
+  g_launches += n;
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "selftest launch: %s", cudaGetErrorString(e));
+  return ok();
+}

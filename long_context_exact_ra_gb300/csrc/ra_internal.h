@@ -1,0 +1,69 @@
+// ra_internal.h — argument bundles shared by the C ABI layer and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ra {
+
+// One attention problem: [B, S, H, D] tensors split into N contiguous virtual shards.
+struct Problem {
+  int B, S, H, D;
+  int N;       // num_shards
+  int Ssh;     // S / N
+  int causal;  // causal_block_size (0 = non-causal)
+  const int32_t* seg;  // [B, S] or nullptr
+};
+
+struct FwdArgs {
+  Problem p;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+};
+
+struct BwdArgs {
+  Problem p;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* out;
+  const float* lse;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_accum;  // [B, S, H, D] fp32 scratch (bf16 path)
+  float* delta;     // [B, H, S]   fp32 scratch
+};
+
+// Launch context: device facts and the device status word.
+struct Ctx {
+  int device;
+  int num_sms;
+  int* status;        // device address of the status word
+  uint64_t limit_ns;  // bounded-wait limit
+  cudaStream_t stream;
+};
+
+// Launchers.  Each returns the CUDA error of its launch(es) and adds the
+// number of kernels it launched to *launches.
+cudaError_t launch_fwd_f32(const FwdArgs& a, const Ctx& c, uint64_t* launches);
+cudaError_t launch_bwd_f32(const BwdArgs& a, const Ctx& c, uint64_t* launches);
+cudaError_t launch_fwd_bf16(const FwdArgs& a, const Ctx& c, uint64_t* launches, const char** why);
+cudaError_t launch_bwd_bf16(const BwdArgs& a, const Ctx& c, uint64_t* launches, const char** why);
+cudaError_t launch_selftest_timeout(const Ctx& c, uint64_t* launches);
+
+// Scratch layout of the bf16 backward (byte offsets into the caller's workspace).
+inline size_t bwd_delta_offset(int B, int S, int H, int D) {
+  size_t dq = (size_t)B * S * H * D * sizeof(float);
+  return (dq + 255) & ~(size_t)255;
+}
+inline size_t bwd_workspace_bytes(int B, int S, int H, int D) {
+  return bwd_delta_offset(B, S, H, D) + (((size_t)B * H * S * sizeof(float) + 255) & ~(size_t)255);
+}
+
+}  // namespace ra

@@ -1,0 +1,167 @@
+"""Thin Python binding of libra.so (include/ra.h).
+
+Argument marshalling only: every step of the attention runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors ([batch, seq, heads, head_dim],
+contiguous); torch provides device memory and the current stream.  If the
+library is missing or fails to load, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libra.so")
+
+RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+RA_F32, RA_BF16 = 0, 1
+_STATUS = {1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "device wait timed out"}
+
+EXPORTS = ("ra_fwd", "ra_bwd", "ra_bwd_workspace_size", "ra_sync_check", "ra_last_error",
+           "ra_kernel_launches", "ra_selftest_timeout")
+
+
+class RAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libra.so once (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with long_context_exact_ra_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.ra_fwd.restype = i32
+    L.ra_fwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    L.ra_bwd.restype = i32
+    L.ra_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                         vp, vp, vp, vp, sz, vp]
+    L.ra_bwd_workspace_size.restype = sz
+    L.ra_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    L.ra_sync_check.restype = i32
+    L.ra_sync_check.argtypes = [vp]
+    L.ra_last_error.restype = ctypes.c_char_p
+    L.ra_last_error.argtypes = []
+    L.ra_kernel_launches.restype = ctypes.c_uint64
+    L.ra_kernel_launches.argtypes = []
+    L.ra_selftest_timeout.restype = i32
+    L.ra_selftest_timeout.argtypes = [ctypes.c_int64, vp]
+    _lib = L
+    return L
+
+
+def _check(status: int):
+    if status != RA_OK:
+        raise RAError(status, lib().ra_last_error().decode())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return RA_F32
+    if t.dtype == torch.bfloat16:
+        return RA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_tensor(name, t, like=None, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if like is not None and (t.shape != like.shape or t.dtype != like.dtype):
+        raise ValueError(f"{name} must match q in shape and dtype")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+
+
+def _chunks(S, num_shards, query_chunk_size, key_chunk_size):
+    ssh = S // num_shards if num_shards > 0 else 0
+    qc = query_chunk_size if query_chunk_size is not None else max(ssh, 1)
+    kc = key_chunk_size if key_chunk_size is not None else max(ssh, 1)
+    return qc, kc
+
+
+def fwd(q, k, v, segment_ids=None, causal_block_size=0, num_shards=1,
+        query_chunk_size=None, key_chunk_size=None, out=None, lse=None, stream=None):
+    """ra_fwd: returns (out [B,S,H,D] like q, lse [B,H,S] float32)."""
+    _check_tensor("q", q)
+    _check_tensor("k", k, q)
+    _check_tensor("v", v, q)
+    B, S, H, D = q.shape
+    if segment_ids is not None:
+        _check_tensor("segment_ids", segment_ids, dtype=torch.int32)
+        if tuple(segment_ids.shape) != (B, S):
+            raise ValueError("segment_ids must be [batch, seq]")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    _check_tensor("out", out, q)
+    _check_tensor("lse", lse, dtype=torch.float32)
+    qc, kc = _chunks(S, num_shards, query_chunk_size, key_chunk_size)
+    _check(lib().ra_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(segment_ids), int(causal_block_size),
+                        int(num_shards), int(qc), int(kc), B, S, H, D, _dtype_code(q),
+                        _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse
+
+
+def bwd_workspace_size(B, S, H, D, dtype) -> int:
+    code = RA_BF16 if dtype == torch.bfloat16 else RA_F32
+    return int(lib().ra_bwd_workspace_size(B, S, H, D, code))
+
+
+def bwd(q, k, v, out, lse, dout, segment_ids=None, causal_block_size=0, num_shards=1,
+        query_chunk_size=None, key_chunk_size=None, dq=None, dk=None, dv=None,
+        workspace=None, stream=None):
+    """ra_bwd: returns (dq, dk, dv), each like q."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _check_tensor(name, t, q)
+    _check_tensor("lse", lse, dtype=torch.float32)
+    B, S, H, D = q.shape
+    if segment_ids is not None:
+        _check_tensor("segment_ids", segment_ids, dtype=torch.int32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    need = bwd_workspace_size(B, S, H, D, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    qc, kc = _chunks(S, num_shards, query_chunk_size, key_chunk_size)
+    _check(lib().ra_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(segment_ids),
+                        int(causal_block_size), int(num_shards), int(qc), int(kc), B, S, H, D,
+                        _dtype_code(q), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dq, dk, dv
+
+
+def sync_check(stream=None):
+    """Synchronize and raise RAError if a kernel reported a timed-out wait."""
+    _check(lib().ra_sync_check(_stream(stream)))
+
+
+def kernel_launches() -> int:
+    return int(lib().ra_kernel_launches())
+
+
+def selftest_timeout(limit_ns: int, stream=None):
+    _check(lib().ra_selftest_timeout(int(limit_ns), _stream(stream)))

@@ -1,0 +1,84 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/ra.h declares, and rejects bad arguments before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from long_context_exact_ra_gb300 import ops
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ra.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(ops.LIB_PATH):
+        from long_context_exact_ra_gb300 import build
+        build.build()
+    return ops.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ra_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(ops.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    # and nothing else with C linkage under the ra_ prefix
+    out = os.popen(f"nm -D --defined-only {ops.LIB_PATH}").read()
+    exported = sorted(set(re.findall(r" T (ra_\w+)", out)))
+    assert exported == declared_functions()
+
+
+def _fwd(L, q=16, k=16, v=16, out=16, lse=16, seg=None, c=0, N=1, qc=1, kc=1, B=1, S=128, H=1, D=64, dt=1):
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return L.ra_fwd(P(q), P(k), P(v), P(seg), c, N, qc, kc, B, S, H, D, dt, P(out), P(lse), None)
+
+
+def test_validation_rejects_bad_arguments(L):
+    assert _fwd(L, q=None) == ops.RA_ERR_INVALID_ARG
+    assert b"q is NULL" in L.ra_last_error()
+    assert _fwd(L, lse=None) == ops.RA_ERR_INVALID_ARG
+    assert _fwd(L, v=24) == ops.RA_ERR_INVALID_ARG  # misaligned
+    assert b"16-byte" in L.ra_last_error()
+    assert _fwd(L, seg=20) == ops.RA_ERR_INVALID_ARG
+    assert _fwd(L, S=130, N=4) == ops.RA_ERR_INVALID_ARG  # seq % num_shards
+    assert _fwd(L, S=128, N=4, qc=3) == ops.RA_ERR_INVALID_ARG  # shard % chunk
+    assert _fwd(L, S=128, N=4, kc=64) == ops.RA_ERR_INVALID_ARG  # 32 % 64
+    assert _fwd(L, c=-1) == ops.RA_ERR_INVALID_ARG
+    assert _fwd(L, N=0) == ops.RA_ERR_INVALID_ARG
+    assert _fwd(L, B=0) == ops.RA_ERR_INVALID_ARG
+    assert _fwd(L, qc=0) == ops.RA_ERR_INVALID_ARG
+    assert _fwd(L, dt=7) == ops.RA_ERR_INVALID_ARG
+    assert _fwd(L, B=1 << 10, S=1 << 12, H=1 << 6, D=128) == ops.RA_ERR_INVALID_ARG  # 2^31 elements
+    assert _fwd(L, D=96) == ops.RA_ERR_UNSUPPORTED  # bf16 only 64 / 128
+    assert _fwd(L, D=256, dt=0) == ops.RA_ERR_UNSUPPORTED
+    # an empty problem succeeds without touching the GPU
+    assert _fwd(L, S=0) == ops.RA_OK
+    assert L.ra_last_error() == b""
+
+
+def test_bwd_validation_and_workspace(L):
+    ws = L.ra_bwd_workspace_size(2, 1000, 3, 128, 1)
+    assert ws >= 2 * 1000 * 3 * 128 * 4 + 2 * 3 * 1000 * 4
+    assert ws % 256 == 0
+    assert L.ra_bwd_workspace_size(2, 1000, 3, 64, 0) >= 2 * 3 * 1000 * 4
+    assert L.ra_bwd_workspace_size(0, 10, 1, 64, 1) == 0
+    P = ctypes.c_void_p
+    args = [P(16)] * 6 + [None, 1, 1, 1, 1, 1, 128, 1, 64, 1, P(16), P(16), P(16), P(16)]
+    st = L.ra_bwd(*args, ctypes.c_size_t(16), None)  # workspace too small
+    assert st == ops.RA_ERR_INVALID_ARG and b"workspace" in L.ra_last_error()
+
+
+def test_selftest_limit_is_validated(L):
+    assert L.ra_selftest_timeout(0, None) == ops.RA_ERR_INVALID_ARG
+    assert L.ra_selftest_timeout(2_000_000_000, None) == ops.RA_ERR_INVALID_ARG
