@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark of blockwise ring attention on GB300 (prints ONE JSON line).
+
+A step is one pass of the whole hot path on the default workload: the causal
+bf16 forward AND backward at batch 1, seq 65536, 32 heads, head_dim 128, 8
+virtual ring shards (ra_fwd then ra_bwd).  The same run also times the
+long-context forward (seq 131072, 32 heads, 16 shards) and reports it under
+"fwd_s131072".  Inputs are seeded synthetic N(0,1) bf16 tensors, resident in
+HBM before the timed region; every input set is larger than the 129 MB L2, so
+no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the full workload on its own GPU as an
+independent replica (the problem's batch x head units shard with no exchange);
+the time is the max over ranks and `value` counts the work of all ranks.
+`--impl reference` times the CPU float64 oracle on the host cores instead
+(rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from long_context_exact_ra_gb300 import flops as F  # noqa: E402
+from long_context_exact_ra_gb300.inputs import WORKLOADS, make_inputs, sample_rows  # noqa: E402
+
+METRIC = "attention TFLOP/s (causal bf16 fwd/bwd, 1xGB300) and % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        mhz, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def source_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "long_context_exact_ra_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(key: str, sha: str):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/*.md, or None
+    if absent or taken on a different kernel source."""
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return None
+    pat = re.compile(r"traffic:\s*key=(\S+)\s+bytes_per_launch=([0-9.eE+]+)\s+source_sha256=(\w+)")
+    for fn in sorted(os.listdir(d)):
+        if not fn.endswith(".md"):
+            continue
+        for line in open(os.path.join(d, fn)):
+            m = pat.search(line)
+            if m and m.group(1) == key and m.group(3) == sha:
+                return float(m.group(2))
+    return None
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def to_dev(x, torch, dev):
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def to_pinned(x, torch):
+    t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    return t.pin_memory()
+
+
+def time_fwd(ops, torch, w, steps, warmup, dev):
+    """Forward-only timing of workload w (device-resident inputs)."""
+    x = make_inputs(w, with_dout=False)
+    q, k, v = (to_dev(getattr(x, n), torch, dev) for n in ("q", "k", "v"))
+    del x
+    out = torch.empty_like(q)
+    lse = torch.empty((w.batch, w.heads, w.seq), dtype=torch.float32, device=dev)
+    args = (None, w.causal_block_size, w.num_shards, w.query_chunk_size, w.key_chunk_size)
+    for _ in range(warmup):
+        ops.fwd(q, k, v, *args, out=out, lse=lse)
+    ops.sync_check()
+    st = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(st)
+        ops.fwd(q, k, v, *args, out=out, lse=lse)
+        b.record(st)
+    torch.cuda.synchronize()
+    ops.sync_check()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    fl = F.fwd_flops_nominal(w.batch, w.seq, w.heads, w.head_dim, w.causal_block_size > 0)
+    return fl, ms
+
+
+def gpu_arm(args, peaks, peaks_src):
+    import torch
+
+    from long_context_exact_ra_gb300 import ops
+
+    ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    ops.lib()
+    w = WORKLOADS[args.workload]
+    backward = w.backward
+    x = make_inputs(w, with_dout=backward)
+    names = ("q", "k", "v") + (("dout",) if backward else ())
+    host = {n: to_pinned(getattr(x, n), torch) for n in names}
+    del x
+    d = {n: host[n].to(dev) for n in names}
+    B, S, H, D = w.shape
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    cargs = (None, w.causal_block_size, w.num_shards, w.query_chunk_size, w.key_chunk_size)
+    if backward:
+        dq, dk, dv = (torch.empty_like(d["q"]) for _ in range(3))
+        wsz = ops.bwd_workspace_size(B, S, H, D, torch.bfloat16)
+        work = torch.empty(wsz, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(rec=None):
+        if rec is not None:
+            rec[0].record(st)
+        ops.fwd(d["q"], d["k"], d["v"], *cargs, out=out, lse=lse)
+        if rec is not None:
+            rec[1].record(st)
+        if backward:
+            ops.bwd(d["q"], d["k"], d["v"], out, lse, d["dout"], *cargs, dq=dq, dk=dk, dv=dv, workspace=work)
+            if rec is not None:
+                rec[2].record(st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ops.sync_check()
+    if ws > 1:
+        torch.distributed.barrier()
+    recs = [(ev(), ev(), ev()) for _ in range(args.steps)]
+    t0, t1 = ev(), ev()
+    launches0 = ops.kernel_launches()
+    try:
+        sel = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        sel = str(local)
+    clocks = ClockSampler(sel)
+    clocks.start()
+    torch.cuda.synchronize()
+    t0.record(st)
+    for i in range(args.steps):
+        step(recs[i])
+    t1.record(st)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    launches = ops.kernel_launches() - launches0
+    ops.sync_check()
+    total_ms = t0.elapsed_time(t1)
+    if ws > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    fwd_ms = statistics.mean(r[0].elapsed_time(r[1]) for r in recs)
+    bwd_ms = statistics.mean(r[1].elapsed_time(r[2]) for r in recs) if backward else 0.0
+    causal = w.causal_block_size > 0
+    fl_f = F.fwd_flops_nominal(B, S, H, D, causal)
+    fl_b = F.bwd_flops_nominal(B, S, H, D, causal) if backward else 0.0
+    per_step = fl_f + fl_b
+    ms_step = total_ms / args.steps
+    value = ws * per_step / (ms_step * 1e-3) / 1e12
+
+    # end-to-end through the public API with host buffers (copies inside the timed region)
+    hout = {n: torch.empty(d["q"].shape, dtype=torch.bfloat16).pin_memory()
+            for n in (("out", "dq", "dk", "dv") if backward else ("out",))}
+    hlse = torch.empty((B, H, S), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        for n in names:
+            d[n].copy_(host[n], non_blocking=True)
+        step()
+        hout["out"].copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        if backward:
+            hout["dq"].copy_(dq, non_blocking=True)
+            hout["dk"].copy_(dk, non_blocking=True)
+            hout["dv"].copy_(dv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(st)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(st)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if ws > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = sum(host[n].numel() * 2 for n in names)
+    d2h = sum(t.numel() * 2 for t in hout.values()) + hlse.numel() * 4
+    ops.sync_check()
+
+    peak = peaks["bf16_tflops"]
+    peak_s = peaks.get("bf16_tflops_sustained", peak)
+    fwd_tf = fl_f / (fwd_ms * 1e-3) / 1e12
+    fwd_sha = source_sha("attn_fwd_sm103.cu", "sm103.cuh")
+    roof_fwd = {"bound": "tensor", "kernel": f"fwd_bf16_kernel<{D}>", "achieved": round(fwd_tf, 1),
+                "peak": peak, "unit": UNIT, "frac": round(fwd_tf / peak, 4),
+                "frac_sustained": round(fwd_tf / peak_s, 4), "peak_source": peaks_src,
+                "traffic": profile_traffic(f"fwd{D}_cfg{args.workload}", fwd_sha),
+                "ms_per_launch": round(fwd_ms, 3), "flops_per_launch": fl_f}
+    roofline = roof_fwd
+    extra = {}
+    if backward:
+        bwd_tf = fl_b / (bwd_ms * 1e-3) / 1e12
+        bwd_sha = source_sha("attn_bwd_sm103.cu", "sm103.cuh")
+        roof_bwd = {"bound": "tensor", "kernel": "ra_bwd (preprocess + main + finalize)",
+                    "achieved": round(bwd_tf, 1), "peak": peak, "unit": UNIT, "frac": round(bwd_tf / peak, 4),
+                    "frac_sustained": round(bwd_tf / peak_s, 4), "peak_source": peaks_src,
+                    "traffic": profile_traffic(f"bwd{D}_cfg{args.workload}", bwd_sha),
+                    "ms_per_launch": round(bwd_ms, 3), "flops_per_launch": fl_b}
+        if bwd_ms >= fwd_ms:
+            roofline, extra["roofline_fwd"] = roof_bwd, roof_fwd
+        else:
+            extra["roofline_bwd"] = roof_bwd
+    # the long-context forward target (seq 131072), same run
+    if args.workload != 4 and not args.no_secondary:
+        del d, host, hout, out, lse
+        if backward:
+            del dq, dk, dv, work
+        torch.cuda.empty_cache()
+        w4 = WORKLOADS[4]
+        fl4, ms4 = time_fwd(ops, torch, w4, max(3, args.steps), args.warmup, dev)
+        tf4 = fl4 / (statistics.mean(ms4) * 1e-3) / 1e12
+        extra["fwd_s131072"] = {"workload": w4.name, "tflops": round(tf4, 1), "frac": round(tf4 / peak, 4),
+                                "frac_sustained": round(tf4 / peak_s, 4), "ms": round(statistics.mean(ms4), 3),
+                                "flops": fl4,
+                                "traffic": profile_traffic("fwd128_cfg4", fwd_sha)}
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, no dataset)",
+        "config": {"workload": w.name, "batch": B, "seq": S, "heads": H, "head_dim": D,
+                   "num_shards": w.num_shards, "causal_block_size": w.causal_block_size,
+                   "query_chunk_size": w.query_chunk_size, "key_chunk_size": w.key_chunk_size,
+                   "step": "ra_fwd + ra_bwd" if backward else "ra_fwd",
+                   "flops_per_step": per_step, "flop_convention": "4*b*h*s*s*d, /2 causal; bwd = 2.5x fwd",
+                   "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{ws}"},
+        "e2e": {"value": round(ws * per_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": launches,
+        "roofline": roofline,
+        "clocks": clk,
+        **extra,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_rows_rate(w, budget_s, x=None, start_rows=32):
+    """Time the float64 oracle on sampled query rows of workload w; return
+    (algorithmic TFLOP/s, rows, seconds, cores)."""
+    import oracle
+
+    if x is None:
+        x = make_inputs(w, with_dout=False)
+    from long_context_exact_ra_gb300.inputs import bf16_bits_to_f32
+    q, k, v = (bf16_bits_to_f32(getattr(x, n)) for n in ("q", "k", "v"))
+    g = np.random.Generator(np.random.PCG64(7))
+    n, total_t, total_f, total_rows = start_rows, 0.0, 0.0, 0
+    c = w.causal_block_size
+    while total_t < budget_s:
+        bh = (int(g.integers(w.batch)), int(g.integers(w.heads)))
+        rows = np.stack([np.full(n, bh[0]), np.full(n, bh[1]), g.integers(w.seq, size=n)], 1)
+        t = time.perf_counter()
+        oracle.ref_fwd_rows(q, k, v, rows, x.segment_ids, c)
+        total_t += time.perf_counter() - t
+        if c > 0:
+            vis = ((rows[:, 2] // c) + 1) * c
+            total_f += 4.0 * w.head_dim * np.minimum(vis, w.seq).sum()
+        else:
+            total_f += 4.0 * w.head_dim * w.seq * n
+        total_rows += n
+        n = min(n * 2, 4096)
+    return total_f / total_t / 1e12, total_rows, total_t, len(os.sched_getaffinity(0))
+
+
+def cpu_baseline(w, budget_s=15.0):
+    tf, rows, secs, cores = oracle_rows_rate(w, budget_s)
+    return {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"float64 oracle forward on {rows} sampled query rows of '{w.name}' "
+                      f"(full key range per row, {secs:.1f} s); algorithmic FLOPs of the visible pairs; "
+                      f"the backward is not sampled (same FLOP convention applies)"}
+
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    x = make_inputs(w, with_dout=False)
+    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_rows_rate(w, per_step, x)
+    rates, secs = [], 0.0
+    for _ in range(args.steps):
+        tf, rows, s, cores = oracle_rows_rate(w, per_step, x)
+        rates.append(tf)
+        secs += s
+    value = statistics.mean(rates)
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded N(0,1) bf16 inputs, computed in float64)",
+           "config": {"workload": w.name, "batch": w.batch, "seq": w.seq, "heads": w.heads,
+                      "head_dim": w.head_dim, "num_shards": w.num_shards},
+           "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": cores,
+                            "sample": f"each step: float64 oracle forward on sampled query rows for "
+                                      f"~{per_step:.0f} s"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, choices=[2, 3, 4, 5], default=5)
+    ap.add_argument("--no-secondary", action="store_true", help="skip the seq-131072 forward line")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    peaks, src = load_peaks()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args, peaks, src)
+
+
+if __name__ == "__main__":
+    main()

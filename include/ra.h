@@ -34,7 +34,7 @@
  * TMA-staged tiles, tcgen05 MMAs accumulating in tensor memory), and dtype
  * RA_F32 with 1 <= head_dim <= 128 (exact fp32 CUDA-core path).
  * Requirements (else RA_ERR_INVALID_ARG): non-NULL tensor pointers, every
- * pointer 16-byte aligned, batch, heads >= 1, seq >= 0, num_shards >= 1,
+ * pointer 16-byte aligned (pointers are not examined when seq = 0), batch, heads >= 1, seq >= 0, num_shards >= 1,
  * seq % num_shards == 0, (seq / num_shards) % query_chunk_size == 0 and
  * % key_chunk_size == 0 (chunk sizes >= 1; seq = 0 is an empty problem and
  * returns RA_OK at once), causal_block_size >= 0, and

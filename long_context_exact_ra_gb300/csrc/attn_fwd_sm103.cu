@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kNInfo; ++i) {
       mbar_init(bars.infofull(i), 1);
-      mbar_init(bars.infoempty(i), 1 + 256);  // MMA thread + every softmax thread
+      mbar_init(bars.infoempty(i), 1 + 8);  // MMA thread + one lane per softmax warp
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(bars.sfull(w), 1);
@@ -488,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!alive) break;
       const Rec r = recs[slot];
       if (r.kind == kRecStop) {
-        mbar_arrive(bars.infoempty(slot));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.infoempty(slot));
         break;
       }
       const int qrow = r.q0 + w * kBM + rl;
@@ -517,9 +518,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!vis) sr[x] = __float_as_uint(-INFINITY);
           }
         }
-        float mx = __uint_as_float(sr[0]);
+        // row max: eight independent chains of three-input max
+        float mx8[8];
 #pragma unroll
-        for (int x = 1; x < 128; ++x) mx = fmaxf(mx, __uint_as_float(sr[x]));
+        for (int c8 = 0; c8 < 8; ++c8) mx8[c8] = fmaxf(__uint_as_float(sr[c8]), __uint_as_float(sr[c8 + 8]));
+#pragma unroll
+        for (int x = 16; x < 128; x += 16) {
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            mx8[c8] = fmax3(mx8[c8], __uint_as_float(sr[x + c8]), __uint_as_float(sr[x + 8 + c8]));
+        }
+        const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
         const float m_tile = mx * sl2;
         float corr = 1.f;
         bool resc = false;
@@ -531,18 +540,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_use = m_tile;
         }
         const float mb = (m_use == -INFINITY) ? 0.f : m_use;
-        float rs = 0.f;
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[64];
 #pragma unroll
         for (int x = 0; x < 64; ++x) {
           const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * x]), sl2, -mb));
           const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * x + 1]), sl2, -mb));
-          rs += p0 + p1;
+          rs4[x & 3] += p0 + p1;
           pk[x] = pack_bf16x2(p0, p1);
+          if (x == 31) tmem_st32(tS, pk);  // first half of P goes out while the rest is computed
         }
-        l = l * corr + rs;
-        tmem_st32(tS, pk);
         tmem_st32(tS + 32, pk + 32);
+        l = l * corr + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
         if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
           for (int cq = 0; cq < D / 32; ++cq) {
@@ -597,7 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = 0.f;
         processed = 0;
       }
-      mbar_arrive(bars.infoempty(slot));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.infoempty(slot));
       ++rec_n;
     }
   }

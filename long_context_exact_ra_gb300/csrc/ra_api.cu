@@ -96,11 +96,11 @@ ra_status validate(const void* const* ptrs, const char* const* names, int nptr,
                 Ssh, qc, kc);
   if (causal_block_size < 0)
     return fail(RA_ERR_INVALID_ARG, "causal_block_size=%d must be >= 0", causal_block_size);
-  for (int i = 0; i < nptr; ++i) {
+  for (int i = 0; i < nptr && S > 0; ++i) {  // an empty problem touches no memory
     if (ptrs[i] == nullptr) return fail(RA_ERR_INVALID_ARG, "%s is NULL", names[i]);
     if (!aligned16(ptrs[i])) return fail(RA_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
   }
-  if (seg != nullptr && !aligned16(seg)) return fail(RA_ERR_INVALID_ARG, "segment_ids is not 16-byte aligned");
+  if (S > 0 && seg != nullptr && !aligned16(seg)) return fail(RA_ERR_INVALID_ARG, "segment_ids is not 16-byte aligned");
   if (dtype == RA_BF16 && D != 64 && D != 128)
     return fail(RA_ERR_UNSUPPORTED, "bf16 path supports head_dim 64 and 128, got %d", D);
   if (dtype == RA_F32 && D > 128) return fail(RA_ERR_UNSUPPORTED, "fp32 path supports head_dim <= 128, got %d", D);

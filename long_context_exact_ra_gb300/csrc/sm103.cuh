@@ -89,6 +89,7 @@ static __device__ __noinline__ bool mbar_wait_impl(uint32_t bar, uint32_t parity
   }
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& c, int site) {
+  if (mbar_test(bar, parity)) return true;  // fast path, no call
   return mbar_wait_impl(bar, parity, c, site, true);
 }
 // Teardown wait: ignores the abort flag (used to let in-flight copies and
@@ -270,6 +271,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
