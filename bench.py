@@ -167,6 +167,53 @@ def time_fwd(ops, torch, w, steps, warmup, dev):
     return fl, ms
 
 
+def run_e2e(args, torch, d, host, names, step, out, lse, backward, grads, st, ws, dev):
+    """Same step through the public API with host buffers: H2D of the inputs from
+    pinned memory, the step, D2H of every result, all inside the timed region."""
+    B, S, H, _ = d["q"].shape
+    hout = {n: torch.empty(d["q"].shape, dtype=torch.bfloat16).pin_memory()
+            for n in (("out", "dq", "dk", "dv") if backward else ("out",))}
+    hlse = torch.empty((B, H, S), dtype=torch.float32).pin_memory()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def e2e_step():
+        for n in names:
+            d[n].copy_(host[n], non_blocking=True)
+        step()
+        hout["out"].copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        if backward:
+            hout["dq"].copy_(grads[0], non_blocking=True)
+            hout["dk"].copy_(grads[1], non_blocking=True)
+            hout["dv"].copy_(grads[2], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(st)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(st)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if ws > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = sum(host[n].numel() * 2 for n in names)
+    d2h = sum(t.numel() * 2 for t in hout.values()) + hlse.numel() * 4
+    return e2e_ms, h2d, d2h
+
+
+def workload_for(args):
+    w = WORKLOADS[args.workload]
+    if args.seq:  # a smaller case of the same workload (profiling); chunks shrink to fit the shard
+        ssh = args.seq // w.num_shards
+        ch = min(w.query_chunk_size, ssh)
+        w = w.with_(name=f"{w.name} at seq {args.seq}", seq=args.seq, query_chunk_size=ch, key_chunk_size=ch)
+    return w
+
+
 def gpu_arm(args, peaks, peaks_src):
     import torch
 
@@ -179,7 +226,7 @@ def gpu_arm(args, peaks, peaks_src):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     ops.lib()
-    w = WORKLOADS[args.workload]
+    w = workload_for(args)
     backward = w.backward
     x = make_inputs(w, with_dout=backward)
     names = ("q", "k", "v") + (("dout",) if backward else ())
@@ -247,37 +294,11 @@ def gpu_arm(args, peaks, peaks_src):
     value = ws * per_step / (ms_step * 1e-3) / 1e12
 
     # end-to-end through the public API with host buffers (copies inside the timed region)
-    hout = {n: torch.empty(d["q"].shape, dtype=torch.bfloat16).pin_memory()
-            for n in (("out", "dq", "dk", "dv") if backward else ("out",))}
-    hlse = torch.empty((B, H, S), dtype=torch.float32).pin_memory()
-
-    def e2e_step():
-        for n in names:
-            d[n].copy_(host[n], non_blocking=True)
-        step()
-        hout["out"].copy_(out, non_blocking=True)
-        hlse.copy_(lse, non_blocking=True)
-        if backward:
-            hout["dq"].copy_(dq, non_blocking=True)
-            hout["dk"].copy_(dk, non_blocking=True)
-            hout["dv"].copy_(dv, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = ev(), ev()
-    e0.record(st)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(st)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if ws > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    h2d = sum(host[n].numel() * 2 for n in names)
-    d2h = sum(t.numel() * 2 for t in hout.values()) + hlse.numel() * 4
-    ops.sync_check()
+    if args.no_e2e:
+        hout, e2e_ms, h2d, d2h = {}, float("nan"), 0, 0
+    else:
+        e2e_ms, h2d, d2h = run_e2e(args, torch, d, host, names, step, out, lse, backward,
+                                   (dq, dk, dv) if backward else None, st, ws, dev)
 
     peak = peaks["bf16_tflops"]
     peak_s = peaks.get("bf16_tflops_sustained", peak)
@@ -325,7 +346,7 @@ def gpu_arm(args, peaks, peaks_src):
                    "step": "ra_fwd + ra_bwd" if backward else "ra_fwd",
                    "flops_per_step": per_step, "flop_convention": "4*b*h*s*s*d, /2 causal; bwd = 2.5x fwd",
                    "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{ws}"},
-        "e2e": {"value": round(ws * per_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+        "e2e": None if args.no_e2e else {"value": round(ws * per_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": launches,
         "roofline": roofline,
@@ -334,6 +355,8 @@ def gpu_arm(args, peaks, peaks_src):
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    if args.seq:
+        result["config"]["note"] = "reduced seq for profiling: not the benchmark workload"
     if ws > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
@@ -381,7 +404,7 @@ def reference_arm(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    w = WORKLOADS[args.workload]
+    w = workload_for(args)
     x = make_inputs(w, with_dout=False)
     per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -415,6 +438,8 @@ def main():
     ap.add_argument("--no-secondary", action="store_true", help="skip the seq-131072 forward line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--seq", type=int, default=0, help="run a smaller seq of the workload (profiling)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

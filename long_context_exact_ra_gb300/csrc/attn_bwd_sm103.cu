@@ -1,9 +1,712 @@
-// attn_bwd_sm103.cu — bf16 backward (placeholder until the tensor-core kernel lands).
+// attn_bwd_sm103.cu — bf16 backward of blockwise ring attention on sm_103a.
+//
+// Gradients of L = sum(dO * out) for out = softmax(Q K^T / sqrt(d)) V with the
+// causal / segment masks of the forward, recomputing P from the saved lse
+// (no S x S matrix is kept; the code walk-through page of Ring Attention,
+// "从论文到代码：深入理解RingAttention的块注意力计算逻辑", names the backward
+// among the implementation's parts and recommends recomputation over saving
+// intermediates, §性能优化技巧 2):
+//   P = exp(S - lse),  Delta_i = <dO_i, O_i>,  dV = P^T dO,
+//   dS = P * (dO V^T - Delta),  dK = dS^T Q / sqrt(d),  dQ = dS K / sqrt(d).
+//
+// Three launches:
+//   1. preprocess: Delta = rowsum(dO * O) and zero the fp32 dQ accumulator
+//   2. main (persistent, one CTA per SM, 14 warps): one unit = one 128-key
+//      K/V tile of one (batch, head).  The unit visits the query tiles in the
+//      order the key block travels around the ring: query shards j = k, k+1,
+//      ... (mod N) ("Ring Attention with Blockwise Transformers for
+//      Near-Infinite Context", paper review page, 环形注意力算法), skipping
+//      tiles with no visible element.  Per (key tile, query tile) pair:
+//        dP^T = V dO^T, S^T = K Q^T          (tcgen05 SS, fp32 in TMEM)
+//        P^T, dS^T by two warpgroups (64 query columns each, one key row per thread)
+//        dV += P^T dO, dK += dS^T Q          (tcgen05 TS: P^T / dS^T read from TMEM)
+//        dQ_tile = dS K                      (tcgen05 SS: dS^T in smem as an MN-major A)
+//      and a dQ warpgroup adds dQ_tile into the fp32 accumulator (vector red.add).
+//   3. finalize: dq = bf16(dQ_accum / sqrt(d)).
+// Tensor memory (512 columns): A | B | dK | dV with A = S^T, later P^T, later
+// dQ_tile; B = dP^T, later dS^T.
+#include <cmath>
+#include <cstdint>
+#include <cudaTypedefs.h>
+
 #include "ra_internal.h"
+#include "sm103.cuh"
 
 namespace ra {
-cudaError_t launch_bwd_bf16(const BwdArgs&, const Ctx&, uint64_t*, const char** why) {
-  *why = "bf16 backward is not built yet";
+
+bool make_tile_map(CUtensorMap* m, const void* ptr, const Problem& p, int rows);
+
+namespace {
+
+constexpr int kT = 128;  // keys per unit tile, queries per pair tile
+constexpr int kNInfo = 8;
+constexpr int kThreads = 448;
+constexpr int kProdWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kDqWarp0 = 10;  // warps 10..13
+
+enum : int { kRecPair = 0, kRecUnitEnd = 1, kRecStop = 2 };
+enum : int { kMasked = 1 };
+
+struct __align__(16) BRec {
+  int kind;
+  int flags;
+  int q0;      // first query row of the tile (global)
+  int qvalid;  // query rows of the tile inside their shard
+  int b, h;
+  int k0;      // first key of the unit tile (global)
+  int kvalid;  // keys of the unit tile inside their shard
+};
+
+template <int D>
+struct BCfg {
+  static constexpr uint32_t TB = kT * D * 2;  // bytes of one [128 x D] bf16 tile
+  static constexpr int QST = 2;               // Q / dO stages
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + TB;
+  static constexpr uint32_t OFF_Q = OFF_V + TB;               // QST stages
+  static constexpr uint32_t OFF_DO = OFF_Q + QST * TB;        // QST stages
+  static constexpr uint32_t OFF_DS = OFF_DO + QST * TB;       // dS^T, 128 x 128 bf16
+  static constexpr uint32_t OFF_VEC = OFF_DS + kT * kT * 2;   // per stage: lse2[128], delta[128]
+  static constexpr uint32_t VEC_BYTES = 2 * kT * 4;
+  static constexpr uint32_t OFF_REC = OFF_VEC + QST * VEC_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_REC + kNInfo * sizeof(BRec);
+  // kvfull, kvempty, qfull[2], qempty[2], infofull[8], infoempty[8], spfull, pready,
+  // dqfull, dqfree, accdone, accfree
+  static constexpr int NBAR = 2 + 2 * QST + 2 * kNInfo + 6;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  // No alignment slack (the D = 128 layout is within a few hundred bytes of the
+  // 227 KB limit): the kernel checks that the dynamic base is 1024-byte aligned.
+  static constexpr uint32_t SMEM = OFF_MISC + 64;
+  static_assert(SMEM <= 232448, "shared memory layout exceeds the per-block limit");
+  static constexpr uint32_t TA = 0, TBc = 128, TDK = 256, TDV = 256 + D;  // TMEM columns
+};
+
+struct BBars {
+  uint32_t base;
+  __device__ uint32_t kvfull() const { return base; }
+  __device__ uint32_t kvempty() const { return base + 8; }
+  __device__ uint32_t qfull(int s) const { return base + 16 + 8 * s; }
+  __device__ uint32_t qempty(int s) const { return base + 32 + 8 * s; }
+  __device__ uint32_t infofull(int i) const { return base + 48 + 8 * i; }
+  __device__ uint32_t infoempty(int i) const { return base + 48 + 8 * (kNInfo + i); }
+  __device__ uint32_t spfull() const { return base + 48 + 16 * kNInfo; }
+  __device__ uint32_t pready() const { return base + 56 + 16 * kNInfo; }
+  __device__ uint32_t dqfull() const { return base + 64 + 16 * kNInfo; }
+  __device__ uint32_t dqfree() const { return base + 72 + 16 * kNInfo; }
+  __device__ uint32_t accdone() const { return base + 80 + 16 * kNInfo; }
+  __device__ uint32_t accfree() const { return base + 88 + 16 * kNInfo; }
+};
+
+struct BwdParams {
+  Problem p;
+  const float* lse;
+  const float* delta;
+  float* dq_accum;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* status;
+  uint64_t limit_ns;
+  int tiles_per_shard;
+  int num_units;
+  float scale;       // 1 / sqrt(D)
+  float scale_log2;  // log2(e) / sqrt(D)
+};
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// 1. preprocess: Delta_i = sum_d dO_id O_id (bf16 inputs, fp32), zero dQ accumulator
+// ---------------------------------------------------------------------------
+__global__ void bwd_pre_kernel(Problem p, const __nv_bfloat16* __restrict__ out,
+                               const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta,
+                               float* __restrict__ dq_accum) {
+  const int warps = blockDim.x / 32;
+  const long long row = (long long)blockIdx.x * warps + threadIdx.x / 32;  // (b, s, h) row
+  const int lane = threadIdx.x & 31;
+  const long long total = (long long)p.B * p.S * p.H;
+  if (row >= total) return;
+  const int h = (int)(row % p.H), s = (int)((row / p.H) % p.S), b = (int)(row / ((long long)p.H * p.S));
+  const size_t base = (size_t)row * p.D;
+  float acc = 0.f;
+  for (int d = lane * 4; d < p.D; d += 128) {
+    const uint2 o = *reinterpret_cast<const uint2*>(out + base + d);
+    const uint2 g = *reinterpret_cast<const uint2*>(dout + base + d);
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float2 of = __bfloat1622float2(o2[i]);
+      const float2 gf = __bfloat1622float2(g2[i]);
+      acc = fmaf(of.x, gf.x, acc);
+      acc = fmaf(of.y, gf.y, acc);
+    }
+    *reinterpret_cast<float4*>(dq_accum + base + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) delta[((size_t)b * p.H + h) * p.S + s] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// 3. finalize: dq = bf16(dq_accum * scale)
+// ---------------------------------------------------------------------------
+__global__ void bwd_fin_kernel(size_t n4, const float4* __restrict__ acc, uint2* __restrict__ dq, float scale) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = acc[i];
+    uint2 o;
+    o.x = pack_bf16x2(a.x * scale, a.y * scale);
+    o.y = pack_bf16x2(a.z * scale, a.w * scale);
+    dq[i] = o;
+  }
+}
+
+// Unit u -> (b, h, key shard k, tile t).  Ordered by increasing key position
+// (largest causal work first), heads and batches interleaved.
+__device__ __forceinline__ void bunit_coords(const BwdParams& P, int u, int& b, int& h, int& k, int& t) {
+  const int BH = P.p.B * P.p.H;
+  const int rank = u / BH, bh = u % BH;
+  k = rank / P.tiles_per_shard;
+  t = rank % P.tiles_per_shard;
+  b = bh / P.p.H;
+  h = bh % P.p.H;
+}
+
+// ---------------------------------------------------------------------------
+// 2. main kernel
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_bf16_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+                    const BwdParams P) {
+  using C = BCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_u32(smem_raw) & 1023u) != 0) {  // swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) atomicCAS(P.status, 0, kDevBadSmem);
+    return;
+  }
+  uint8_t* sm = smem_raw;
+  const uint32_t sbase = smem_u32(sm);
+  BRec* recs = reinterpret_cast<BRec*>(sm + C::OFF_REC);
+  BBars bars{sbase + C::OFF_BAR};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Problem& pb = P.p;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bars.kvfull(), 1);
+    mbar_init(bars.kvempty(), 1);
+    for (int s = 0; s < C::QST; ++s) {
+      mbar_init(bars.qfull(s), 1);
+      mbar_init(bars.qempty(s), 1);
+    }
+    for (int i = 0; i < kNInfo; ++i) {
+      mbar_init(bars.infofull(i), 1);
+      mbar_init(bars.infoempty(i), 1 + 8 + 4);  // MMA + softmax warps + dQ warps
+    }
+    mbar_init(bars.spfull(), 1);
+    mbar_init(bars.pready(), 256);
+    mbar_init(bars.dqfull(), 1);
+    mbar_init(bars.dqfree(), 128);
+    mbar_init(bars.accdone(), 1);
+    mbar_init(bars.accfree(), 256);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  WaitCtl ctl{P.status, abort_flag, P.limit_ns};
+
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+      tma_prefetch_desc(&mdo);
+    }
+    int rec_n = 0, pair_n = 0, unit_n = 0, kv_loads = 0;
+    bool alive = true;
+    const int c = pb.causal;
+    auto publish = [&](const BRec& r) -> bool {
+      const int slot = rec_n % kNInfo;
+      if (!mbar_wait(bars.infoempty(slot), ((rec_n / kNInfo) & 1) ^ 1, ctl, 40)) return false;
+      recs[slot] = r;
+      mbar_arrive(bars.infofull(slot));
+      ++rec_n;
+      return true;
+    };
+    for (int u = blockIdx.x; u < P.num_units && alive; u += gridDim.x) {
+      int b, h, k, t;
+      bunit_coords(P, u, b, h, k, t);
+      const int k0 = k * pb.Ssh + t * kT;
+      const int kvalid = min(kT, (k + 1) * pb.Ssh - k0);
+      const int klast = k0 + kvalid - 1;
+      int kmn = 0, kmx = 0;
+      if (pb.seg) {
+        int mn = INT_MAX, mx = INT_MIN;
+        for (int r = lane; r < kvalid; r += 32) {
+          const int sv = __ldg(pb.seg + (size_t)b * pb.S + k0 + r);
+          mn = min(mn, sv);
+          mx = max(mx, sv);
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+          mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+          mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        kmn = mn;
+        kmx = mx;
+      }
+      if (lane == 0) {
+        alive = mbar_wait(bars.kvempty(), (unit_n & 1) ^ 1, ctl, 41);
+        if (alive) {
+          ++kv_loads;
+          mbar_arrive_expect_tx(bars.kvfull(), 2 * C::TB);
+          for (int cb = 0; cb < D / 64; ++cb) {
+            tma_load_4d(sbase + C::OFF_K + cb * 16384, &mk, bars.kvfull(), cb * 64, h, k0, b);
+            tma_load_4d(sbase + C::OFF_V + cb * 16384, &mv, bars.kvfull(), cb * 64, h, k0, b);
+          }
+        }
+      }
+      alive = __shfl_sync(0xffffffffu, alive, 0);
+      for (int i = 0; i < pb.N && alive; ++i) {
+        const int js = (k + i) % pb.N;  // the ring device holding this key block at step i
+        const int qbeg = js * pb.Ssh, qend = qbeg + pb.Ssh;
+        if (c > 0 && (qend - 1) / c < k0 / c) continue;  // every query of the shard precedes the keys
+        for (int t0 = 0; t0 < P.tiles_per_shard && alive; t0 += 32) {
+          int qmn = 0, qmx = 0;
+          const int my_t = t0 + lane;
+          if (pb.seg && my_t < P.tiles_per_shard) {
+            const int qa = qbeg + my_t * kT;
+            const int qb = min(qend, qa + kT);
+            int mn = INT_MAX, mx = INT_MIN;
+            if (!(c > 0 && (qb - 1) / c < k0 / c)) {
+              const int* sp = pb.seg + (size_t)b * pb.S;
+              for (int x = qa; x < qb; ++x) {
+                const int sv = __ldg(sp + x);
+                mn = min(mn, sv);
+                mx = max(mx, sv);
+              }
+            }
+            qmn = mn;
+            qmx = mx;
+          }
+          const int tend = min(32, P.tiles_per_shard - t0);
+          for (int tt = 0; tt < tend && alive; ++tt) {
+            const int qa = qbeg + (t0 + tt) * kT;
+            const int qvalid = min(kT, qend - qa);
+            const int ql = qa + qvalid - 1;
+            const int tmn = __shfl_sync(0xffffffffu, qmn, tt);
+            const int tmx = __shfl_sync(0xffffffffu, qmx, tt);
+            bool skip = false, full = true;
+            if (c > 0) {
+              if (ql / c < k0 / c) skip = true;
+              else if (!(qa / c >= klast / c)) full = false;
+            }
+            if (!skip && pb.seg) {
+              if (tmx < kmn || tmn > kmx) skip = true;
+              else if (!(kmn == kmx && tmn == kmx && tmx == kmx)) full = false;
+            }
+            if (qvalid < kT || kvalid < kT) full = false;
+            if (skip) continue;
+            // stage: lse2, delta, query segment ids (plain loads), then Q and dO by TMA
+            const int s = pair_n % C::QST;
+            const uint32_t par = ((pair_n / C::QST) & 1) ^ 1;
+            if (lane == 0) alive = mbar_wait(bars.qempty(s), par, ctl, 42);
+            alive = __shfl_sync(0xffffffffu, alive, 0);
+            if (!alive) break;
+            float* vec = reinterpret_cast<float*>(sm + C::OFF_VEC + s * C::VEC_BYTES);
+            const size_t lrow = ((size_t)b * pb.H + h) * pb.S;
+            for (int r = lane; r < kT; r += 32) {
+              const int q = qa + r;
+              const bool in = r < qvalid;
+              const float l = in ? __ldg(P.lse + lrow + q) : 0.f;
+              vec[r] = l * 1.4426950408889634f;
+              vec[kT + r] = in ? __ldg(P.delta + lrow + q) : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive_expect_tx(bars.qfull(s), 2 * C::TB);
+              for (int cb = 0; cb < D / 64; ++cb) {
+                tma_load_4d(sbase + C::OFF_Q + s * C::TB + cb * 16384, &mq, bars.qfull(s), cb * 64, h, qa, b);
+                tma_load_4d(sbase + C::OFF_DO + s * C::TB + cb * 16384, &mdo, bars.qfull(s), cb * 64, h, qa, b);
+              }
+              BRec r;
+              r.kind = kRecPair;
+              r.flags = full ? 0 : kMasked;
+              r.q0 = qa;
+              r.qvalid = qvalid;
+              r.b = b;
+              r.h = h;
+              r.k0 = k0;
+              r.kvalid = kvalid;
+              alive = publish(r);
+            }
+            alive = __shfl_sync(0xffffffffu, alive, 0);
+            ++pair_n;
+          }
+        }
+      }
+      if (lane == 0 && alive) {
+        BRec r;
+        r.kind = kRecUnitEnd;
+        r.flags = 0;
+        r.q0 = 0;
+        r.qvalid = 0;
+        r.b = b;
+        r.h = h;
+        r.k0 = k0;
+        r.kvalid = kvalid;
+        alive = publish(r);
+      }
+      alive = __shfl_sync(0xffffffffu, alive, 0);
+      ++unit_n;
+    }
+    if (lane == 0 && alive) {
+      BRec r;
+      r.kind = kRecStop;
+      publish(r);
+    }
+    if (lane == 0) {  // let issued copies land (bounded, ignores abort)
+      for (int s = 0; s < C::QST; ++s) {
+        if (pair_n <= s) continue;
+        const int last = s + ((pair_n - 1 - s) / C::QST) * C::QST;
+        mbar_drain(bars.qfull(s), (last / C::QST) & 1, ctl, 43);
+      }
+      if (kv_loads > 0) mbar_drain(bars.kvfull(), (kv_loads - 1) & 1, ctl, 44);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idSP = idesc_bf16_f32(kT, kT, 0, 0);  // S^T, dP^T: K-major A and B
+      constexpr uint32_t idKV = idesc_bf16_f32(kT, D, 0, 1);   // dV, dK: A in TMEM, B MN-major
+      constexpr uint32_t idQ = idesc_bf16_f32(kT, D, 1, 1);    // dQ: A (dS^T smem) and B MN-major
+      int rec_n = 0, pair_n = 0, unit_n = 0, dq_n = 0, unit_pairs = 0;
+      uint32_t pready_ph = 0;
+      bool alive = true, in_unit = false;
+      const uint32_t tA = tbase + C::TA, tB = tbase + C::TBc;
+      while (alive) {
+        const int slot = rec_n % kNInfo;
+        if (!mbar_wait(bars.infofull(slot), (rec_n / kNInfo) & 1, ctl, 50)) break;
+        const BRec r = recs[slot];
+        if (r.kind == kRecStop) {
+          mbar_arrive(bars.infoempty(slot));
+          break;
+        }
+        if (!in_unit) {  // first record of a unit: its K/V tiles must be resident
+          if (!mbar_wait(bars.kvfull(), unit_n & 1, ctl, 51)) break;
+          in_unit = true;
+          unit_pairs = 0;
+        }
+        if (r.kind == kRecUnitEnd) {
+          mma_commit(bars.accdone());
+          mma_commit(bars.kvempty());
+          mbar_arrive(bars.infoempty(slot));
+          ++rec_n;
+          ++unit_n;
+          in_unit = false;
+          continue;
+        }
+        const bool first = unit_pairs == 0;
+        const int s = pair_n % C::QST;
+        if (!mbar_wait(bars.qfull(s), (pair_n / C::QST) & 1, ctl, 52)) break;
+        tc_fence_after();
+        const uint32_t kS = sbase + C::OFF_K, vS = sbase + C::OFF_V;
+        const uint32_t qS = sbase + C::OFF_Q + s * C::TB, doS = sbase + C::OFF_DO + s * C::TB;
+        // dP^T = V dO^T into B (B was last read by the previous pair's dK MMA: in order)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tB, sdesc_sw128(vS + off, 16, 1024), sdesc_sw128(doS + off, 16, 1024), idSP, kk > 0);
+        }
+        // S^T = K Q^T into A, once the previous dQ tile has been read out of A
+        if (dq_n > 0 && !mbar_wait(bars.dqfree(), (dq_n - 1) & 1, ctl, 53)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tA, sdesc_sw128(kS + off, 16, 1024), sdesc_sw128(qS + off, 16, 1024), idSP, kk > 0);
+        }
+        mma_commit(bars.spfull());
+        // wait for P^T, dS^T (TMEM) and dS^T (smem)
+        if (!mbar_wait(bars.pready(), pready_ph, ctl, 54)) break;
+        pready_ph ^= 1;
+        // the previous unit's dK / dV must have been read out before they are overwritten
+        if (first && unit_n > 0 && !mbar_wait(bars.accfree(), (unit_n - 1) & 1, ctl, 55)) break;
+        tc_fence_after();
+        // dV += P^T dO ; dK += dS^T Q   (K = 128 queries: columns 0-31 and 64-95 of A / B)
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk) {
+          const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+          mma_ts(tbase + C::TDV, tA + acol, sdesc_sw128(doS + kk * 2048, 16384, 1024), idKV,
+                 (first && kk == 0) ? 0 : 1);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk) {
+          const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+          mma_ts(tbase + C::TDK, tB + acol, sdesc_sw128(qS + kk * 2048, 16384, 1024), idKV,
+                 (first && kk == 0) ? 0 : 1);
+        }
+        // dQ_tile = dS K into A (overwrites P^T after the dV MMA read it: in order)
+        const uint32_t dsS = sbase + C::OFF_DS;
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_ss(tA, sdesc_sw128(dsS + kk * 2048, 16384, 1024), sdesc_sw128(kS + kk * 2048, 16384, 1024), idQ,
+                 kk > 0);
+        mma_commit(bars.dqfull());
+        mma_commit(bars.qempty(s));
+        ++dq_n;
+        ++pair_n;
+        ++unit_pairs;
+        mbar_arrive(bars.infoempty(slot));
+        ++rec_n;
+      }
+      // drain every MMA before TMEM is freed
+      mma_commit(bars.kvempty());
+      mbar_drain(bars.kvempty(), unit_n & 1, ctl, 56);
+    }
+    __syncwarp();
+  } else if (warp >= kDqWarp0) {
+    // ------------------------------------------------------------------ dQ accumulation
+    const int q4 = warp & 3;  // TMEM lanes 32*q4 .. (the dQ tile's query rows)
+    const int row = q4 * 32 + lane;
+    const uint32_t tA = tbase + C::TA + ((uint32_t)(q4 * 32) << 16);
+    int rec_n = 0;
+    uint32_t dq_ph = 0;
+    bool alive = true;
+    while (alive) {
+      const int slot = rec_n % kNInfo;
+      alive = __all_sync(0xffffffffu, mbar_wait(bars.infofull(slot), (rec_n / kNInfo) & 1, ctl, 60));
+      if (!alive) break;
+      const BRec r = recs[slot];
+      if (r.kind == kRecStop) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.infoempty(slot));
+        break;
+      }
+      if (r.kind == kRecPair) {
+        alive = __all_sync(0xffffffffu, mbar_wait(bars.dqfull(), dq_ph, ctl, 61));
+        if (!alive) break;
+        dq_ph ^= 1;
+        tc_fence_after();
+        float* dst = P.dq_accum + (((size_t)r.b * pb.S + r.q0 + row) * pb.H + r.h) * D;
+        const bool mine = row < r.qvalid;
+        constexpr int HD = D / 2;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[HD];
+#pragma unroll
+          for (int cq = 0; cq < HD / 32; ++cq) tmem_ld32(tA + hh * HD + cq * 32, v + cq * 32);
+#pragma unroll
+          for (int cq = 0; cq < HD / 32; ++cq) tmem_ld_wait(v + cq * 32);
+          if (hh == 1) {  // the whole tile is in registers: release tensor memory
+            tc_fence_before();
+            mbar_arrive(bars.dqfree());
+          }
+          if (mine) {
+#pragma unroll
+            for (int x = 0; x < HD; x += 4)
+              red_add_v4(dst + hh * HD + x, __uint_as_float(v[x]), __uint_as_float(v[x + 1]),
+                         __uint_as_float(v[x + 2]), __uint_as_float(v[x + 3]));
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.infoempty(slot));
+      ++rec_n;
+    }
+  } else {
+    // ------------------------------------------------------------------ P / dS warpgroups
+    const int wg = warp >> 2;              // query columns 64*wg .. +63
+    const int r4 = warp & 3;
+    const int kr = r4 * 32 + lane;         // key row within the unit tile
+    const uint32_t lane_off = (uint32_t)(r4 * 32) << 16;
+    const uint32_t tA = tbase + C::TA + lane_off, tB = tbase + C::TBc + lane_off;
+    const float sl2 = P.scale_log2;
+    int rec_n = 0, pair_n = 0, unit_pairs = 0;
+    uint32_t sp_ph = 0, acc_ph = 0;
+    bool alive = true;
+    uint8_t* dsT = sm + C::OFF_DS + wg * 16384;  // this warpgroup's 64-query block of dS^T
+    while (alive) {
+      const int slot = rec_n % kNInfo;
+      alive = __all_sync(0xffffffffu, mbar_wait(bars.infofull(slot), (rec_n / kNInfo) & 1, ctl, 70));
+      if (!alive) break;
+      const BRec r = recs[slot];
+      if (r.kind == kRecStop) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.infoempty(slot));
+        break;
+      }
+      if (r.kind == kRecPair) {
+        const int s = pair_n % C::QST;
+        const float* vec = reinterpret_cast<const float*>(sm + C::OFF_VEC + s * C::VEC_BYTES);
+        const int* qsegp = pb.seg ? pb.seg + (size_t)r.b * pb.S : nullptr;
+        alive = __all_sync(0xffffffffu, mbar_wait(bars.spfull(), sp_ph, ctl, 71));
+        if (!alive) break;
+        sp_ph ^= 1;
+        tc_fence_after();
+        const bool masked = r.flags & kMasked;
+        const int kpos = r.k0 + kr;
+        const int cb = pb.causal;
+        const int kblk = cb > 0 ? kpos / cb : 0;
+        const int kseg = (pb.seg && kr < r.kvalid) ? __ldg(pb.seg + (size_t)r.b * pb.S + kpos) : 0;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int c0 = wg * 64 + half * 32;  // first query column of this chunk
+          uint32_t sv[32], dp[32];
+          tmem_ld32(tA + c0, sv);
+          tmem_ld32(tB + c0, dp);
+          tmem_ld_wait(sv);
+          tmem_ld_wait(dp);
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int x = 0; x < 32; x += 2) {
+            float pp[2], dd[2];
+#pragma unroll
+            for (int y = 0; y < 2; ++y) {
+              const int cc = c0 + x + y;
+              float p = ex2_approx(fmaf(__uint_as_float(sv[x + y]), sl2, -vec[cc]));
+              if (masked) {
+                const int qpos = r.q0 + cc;
+                bool vis = (kr < r.kvalid) && (cc < r.qvalid);
+                if (cb > 0) vis = vis && (qpos / cb >= kblk);
+                if (qsegp) vis = vis && (__ldg(qsegp + min(qpos, pb.S - 1)) == kseg);
+                if (!vis) p = 0.f;
+              }
+              pp[y] = p;
+              dd[y] = p * (__uint_as_float(dp[x + y]) - vec[kT + cc]);
+            }
+            pk[x / 2] = pack_bf16x2(pp[0], pp[1]);
+            dk[x / 2] = pack_bf16x2(dd[0], dd[1]);
+          }
+          // P^T and dS^T (bf16 pairs) over the columns this chunk came from
+          tmem_st16(tA + wg * 64 + half * 16, pk);
+          tmem_st16(tB + wg * 64 + half * 16, dk);
+          // dS^T into smem: row kr, queries c0..c0+31 of this block (128B swizzle)
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const int chunk = half * 4 + ch;  // 16-byte chunk within the 128-byte row
+            uint4 val = make_uint4(dk[ch * 4], dk[ch * 4 + 1], dk[ch * 4 + 2], dk[ch * 4 + 3]);
+            *reinterpret_cast<uint4*>(dsT + kr * 128 + ((chunk ^ (kr & 7)) * 16)) = val;
+          }
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bars.pready());
+        ++pair_n;
+        ++unit_pairs;
+      } else if (r.kind == kRecUnitEnd) {
+        // dK (warpgroup 0) or dV (warpgroup 1) rows -> bf16
+        alive = __all_sync(0xffffffffu, mbar_wait(bars.accdone(), acc_ph, ctl, 72));
+        if (!alive) break;
+        acc_ph ^= 1;
+        tc_fence_after();
+        const uint32_t tacc = tbase + (wg == 0 ? C::TDK : C::TDV) + lane_off;
+        const float mul = wg == 0 ? P.scale : 1.f;
+        __nv_bfloat16* dst = (wg == 0 ? P.dk : P.dv) + (((size_t)r.b * pb.S + r.k0 + kr) * pb.H + r.h) * D;
+#pragma unroll
+        for (int cq = 0; cq < D / 32; ++cq) {
+          uint32_t o[32];
+          tmem_ld32(tacc + cq * 32, o);
+          tmem_ld_wait(o);
+          if (unit_pairs == 0) {  // no visible query: the gradient is zero
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = 0u;
+          }
+          if (kr < r.kvalid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cq * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 val;
+              val.x = pack_bf16x2(__uint_as_float(o[v4 * 8 + 0]) * mul, __uint_as_float(o[v4 * 8 + 1]) * mul);
+              val.y = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2]) * mul, __uint_as_float(o[v4 * 8 + 3]) * mul);
+              val.z = pack_bf16x2(__uint_as_float(o[v4 * 8 + 4]) * mul, __uint_as_float(o[v4 * 8 + 5]) * mul);
+              val.w = pack_bf16x2(__uint_as_float(o[v4 * 8 + 6]) * mul, __uint_as_float(o[v4 * 8 + 7]) * mul);
+              d4[v4] = val;
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bars.accfree());
+        unit_pairs = 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.infoempty(slot));
+      ++rec_n;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tbase, 512);
+}
+
+}  // namespace
+
+template <int D>
+static cudaError_t launch_bwd_bf16_d(const BwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
+  using Cf = BCfg<D>;
+  const Problem& p = a.p;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_tile_map(&mq, a.q, p, kT) || !make_tile_map(&mk, a.k, p, kT) || !make_tile_map(&mv, a.v, p, kT) ||
+      !make_tile_map(&mdo, a.dout, p, kT)) {
+    *why = "cuTensorMapEncodeTiled failed (driver entry point unavailable or tensor rejected)";
+    return cudaSuccess;
+  }
+  const long long rows = (long long)p.B * p.S * p.H;
+  bwd_pre_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, c.stream>>>(p, (const __nv_bfloat16*)a.out,
+                                                                   (const __nv_bfloat16*)a.dout, a.delta,
+                                                                   a.dq_accum);
+  *launches += 1;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  BwdParams P;
+  P.p = p;
+  P.lse = a.lse;
+  P.delta = a.delta;
+  P.dq_accum = a.dq_accum;
+  P.dk = (__nv_bfloat16*)a.dk;
+  P.dv = (__nv_bfloat16*)a.dv;
+  P.status = c.status;
+  P.limit_ns = c.limit_ns;
+  P.tiles_per_shard = (p.Ssh + kT - 1) / kT;
+  P.num_units = p.B * p.H * p.N * P.tiles_per_shard;
+  P.scale = (float)(1.0 / sqrt((double)p.D));
+  P.scale_log2 = (float)(1.4426950408889634 / sqrt((double)p.D));
+  static bool attr_set[256][2];
+  const int di = D == 64 ? 0 : 1;
+  if (!attr_set[c.device][di]) {
+    e = cudaFuncSetAttribute(bwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[c.device][di] = true;
+  }
+  const int grid = std::min(c.num_sms, P.num_units);
+  bwd_bf16_kernel<D><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, mdo, P);
+  *launches += 1;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t n4 = (size_t)rows * p.D / 4;
+  bwd_fin_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(n4, (const float4*)a.dq_accum, (uint2*)a.dq, P.scale);
+  *launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_bf16(const BwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
+  if (a.p.D == 64) return launch_bwd_bf16_d<64>(a, c, launches, why);
+  if (a.p.D == 128) return launch_bwd_bf16_d<128>(a, c, launches, why);
+  *why = "bf16 head_dim must be 64 or 128";
   return cudaSuccess;
 }
+
 }  // namespace ra

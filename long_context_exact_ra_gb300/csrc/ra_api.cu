@@ -216,6 +216,7 @@ RA_API ra_status ra_sync_check(void* stream) {
   if (word != 0) {
     int zero = 0;
     cudaMemcpy(c.status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (word & 0x20000) return fail(RA_ERR_CUDA, "a kernel found its shared memory misaligned and did nothing");
     return fail(RA_ERR_TIMEOUT, "a device-side wait ran out (site %d)", word & 0xFFFF);
   }
   return ok();

@@ -15,6 +15,7 @@ namespace ra {
 // Device status word (timeouts).  Value = kDevTimeout | site.
 // ---------------------------------------------------------------------------
 constexpr int kDevTimeout = 0x10000;
+constexpr int kDevBadSmem = 0x20000;  // dynamic shared memory not 1024-byte aligned
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
