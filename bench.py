@@ -125,6 +125,22 @@ def profile_traffic(key: str, sha: str):
     return None
 
 
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """Max of a per-rank scalar (step time) over all ranks; identity on one rank."""
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(ws: int, flops_per_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every replica does flops_per_step in the (max-over-ranks) step time."""
+    return ws * flops_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -195,11 +211,7 @@ def run_e2e(args, torch, d, host, names, step, out, lse, backward, grads, st, ws
         e2e_step()
     e1.record(st)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if ws > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
     h2d = sum(host[n].numel() * 2 for n in names)
     d2h = sum(t.numel() * 2 for t in hout.values()) + hlse.numel() * 4
     return e2e_ms, h2d, d2h
@@ -279,11 +291,7 @@ def gpu_arm(args, peaks, peaks_src):
     clk = clocks.stop()
     launches = ops.kernel_launches() - launches0
     ops.sync_check()
-    total_ms = t0.elapsed_time(t1)
-    if ws > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), ws, dev)
     fwd_ms = statistics.mean(r[0].elapsed_time(r[1]) for r in recs)
     bwd_ms = statistics.mean(r[1].elapsed_time(r[2]) for r in recs) if backward else 0.0
     causal = w.causal_block_size > 0
@@ -291,11 +299,11 @@ def gpu_arm(args, peaks, peaks_src):
     fl_b = F.bwd_flops_nominal(B, S, H, D, causal) if backward else 0.0
     per_step = fl_f + fl_b
     ms_step = total_ms / args.steps
-    value = ws * per_step / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(ws, per_step, ms_step)
 
     # end-to-end through the public API with host buffers (copies inside the timed region)
     if args.no_e2e:
-        hout, e2e_ms, h2d, d2h = {}, float("nan"), 0, 0
+        e2e_ms, h2d, d2h = float("nan"), 0, 0
     else:
         e2e_ms, h2d, d2h = run_e2e(args, torch, d, host, names, step, out, lse, backward,
                                    (dq, dk, dv) if backward else None, st, ws, dev)
@@ -325,7 +333,7 @@ def gpu_arm(args, peaks, peaks_src):
             extra["roofline_bwd"] = roof_bwd
     # the long-context forward target (seq 131072), same run
     if args.workload != 4 and not args.no_secondary:
-        del d, host, hout, out, lse
+        del d, host, out, lse
         if backward:
             del dq, dk, dv, work
         torch.cuda.empty_cache()
@@ -346,7 +354,7 @@ def gpu_arm(args, peaks, peaks_src):
                    "step": "ra_fwd + ra_bwd" if backward else "ra_fwd",
                    "flops_per_step": per_step, "flop_convention": "4*b*h*s*s*d, /2 causal; bwd = 2.5x fwd",
                    "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{ws}"},
-        "e2e": None if args.no_e2e else {"value": round(ws * per_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+        "e2e": None if args.no_e2e else {"value": round(whole_job_tflops(ws, per_step, e2e_ms), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": launches,
         "roofline": roofline,

@@ -10,8 +10,8 @@
 //   dS = P * (dO V^T - Delta),  dK = dS^T Q / sqrt(d),  dQ = dS K / sqrt(d).
 //
 // Three launches:
-//   1. preprocess: Delta = rowsum(dO * O) and zero the fp32 dQ accumulator
-//   2. main (persistent, one CTA per SM, 14 warps): one unit = one 128-key
+//   1. preprocess: Delta = rowsum(dO * O) next to lse * log2(e); zero the fp32 dQ accumulator
+//   2. main (persistent, one CTA per SM, 10 warps): one unit = one 128-key
 //      K/V tile of one (batch, head).  The unit visits the query tiles in the
 //      order the key block travels around the ring: query shards j = k, k+1,
 //      ... (mod N) ("Ring Attention with Blockwise Transformers for
@@ -20,8 +20,8 @@
 //        dP^T = V dO^T, S^T = K Q^T          (tcgen05 SS, fp32 in TMEM)
 //        P^T, dS^T by two warpgroups (64 query columns each, one key row per thread)
 //        dV += P^T dO, dK += dS^T Q          (tcgen05 TS: P^T / dS^T read from TMEM)
-//        dQ_tile = dS K                      (tcgen05 SS: dS^T in smem as an MN-major A)
-//      and a dQ warpgroup adds dQ_tile into the fp32 accumulator (vector red.add).
+//        dQ^T = K^T dS^T                     (tcgen05 SS: dS^T in smem as an MN-major B)
+//      and the same two warpgroups add the dQ tile into the fp32 accumulator.
 //   3. finalize: dq = bf16(dQ_accum / sqrt(d)).
 // Tensor memory (512 columns): A | B | dK | dV with A = S^T, later P^T, later
 // dQ_tile; B = dP^T, later dS^T.
@@ -40,10 +40,9 @@ namespace {
 
 constexpr int kT = 128;  // keys per unit tile, queries per pair tile
 constexpr int kNInfo = 8;
-constexpr int kThreads = 448;
+constexpr int kThreads = 320;
 constexpr int kProdWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kDqWarp0 = 10;  // warps 10..13
 
 enum : int { kRecPair = 0, kRecUnitEnd = 1, kRecStop = 2 };
 enum : int { kMasked = 1 };
@@ -67,8 +66,8 @@ struct BCfg {
   static constexpr uint32_t OFF_Q = OFF_V + TB;               // QST stages
   static constexpr uint32_t OFF_DO = OFF_Q + QST * TB;        // QST stages
   static constexpr uint32_t OFF_DS = OFF_DO + QST * TB;       // dS^T, 128 x 128 bf16
-  static constexpr uint32_t OFF_VEC = OFF_DS + kT * kT * 2;   // per stage: lse2[128], delta[128]
-  static constexpr uint32_t VEC_BYTES = 2 * kT * 4;
+  static constexpr uint32_t OFF_VEC = OFF_DS + kT * kT * 2;   // per stage: 130 (lse2, delta) pairs
+  static constexpr uint32_t VEC_BYTES = kBwdVecEntries * 8;
   static constexpr uint32_t OFF_REC = OFF_VEC + QST * VEC_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_REC + kNInfo * sizeof(BRec);
   // kvfull, kvempty, qfull[2], qempty[2], infofull[8], infoempty[8], spfull, pready,
@@ -100,8 +99,8 @@ struct BBars {
 
 struct BwdParams {
   Problem p;
-  const float* lse;
-  const float* delta;
+  const float2* ld2;  // (lse * log2(e), Delta) per (b, h, s), row pitch Sp
+  int Sp;
   float* dq_accum;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -113,17 +112,21 @@ struct BwdParams {
   float scale_log2;  // log2(e) / sqrt(D)
 };
 
+__device__ __forceinline__ void red_add_f32(float* addr, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+}
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
 
 // ---------------------------------------------------------------------------
-// 1. preprocess: Delta_i = sum_d dO_id O_id (bf16 inputs, fp32), zero dQ accumulator
+// 1. preprocess: Delta_i = sum_d dO_id O_id (bf16 inputs, fp32) stored next to
+//    lse_i * log2(e), and the dQ accumulator zeroed
 // ---------------------------------------------------------------------------
 __global__ void bwd_pre_kernel(Problem p, const __nv_bfloat16* __restrict__ out,
-                               const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta,
-                               float* __restrict__ dq_accum) {
+                               const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
+                               float2* __restrict__ ld2, int Sp, float* __restrict__ dq_accum) {
   const int warps = blockDim.x / 32;
   const long long row = (long long)blockIdx.x * warps + threadIdx.x / 32;  // (b, s, h) row
   const int lane = threadIdx.x & 31;
@@ -148,7 +151,10 @@ __global__ void bwd_pre_kernel(Problem p, const __nv_bfloat16* __restrict__ out,
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) delta[((size_t)b * p.H + h) * p.S + s] = acc;
+  if (lane == 0) {
+    const size_t bh = (size_t)b * p.H + h;
+    ld2[bh * Sp + s] = make_float2(lse[bh * p.S + s] * 1.4426950408889634f, acc);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -208,12 +214,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kNInfo; ++i) {
       mbar_init(bars.infofull(i), 1);
-      mbar_init(bars.infoempty(i), 1 + 8 + 4);  // MMA + softmax warps + dQ warps
+      mbar_init(bars.infoempty(i), 1 + 8);  // MMA thread + one lane per P/dS warp
     }
     mbar_init(bars.spfull(), 1);
     mbar_init(bars.pready(), 256);
     mbar_init(bars.dqfull(), 1);
-    mbar_init(bars.dqfree(), 128);
+    mbar_init(bars.dqfree(), 256);
     mbar_init(bars.accdone(), 1);
     mbar_init(bars.accfree(), 256);
     fence_mbar_init();
@@ -320,28 +326,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (qvalid < kT || kvalid < kT) full = false;
             if (skip) continue;
-            // stage: lse2, delta, query segment ids (plain loads), then Q and dO by TMA
+            // stage s: Q and dO tiles (TMA) and the (lse2, delta) pairs of the tile (bulk copy)
             const int s = pair_n % C::QST;
             const uint32_t par = ((pair_n / C::QST) & 1) ^ 1;
             if (lane == 0) alive = mbar_wait(bars.qempty(s), par, ctl, 42);
             alive = __shfl_sync(0xffffffffu, alive, 0);
             if (!alive) break;
-            float* vec = reinterpret_cast<float*>(sm + C::OFF_VEC + s * C::VEC_BYTES);
-            const size_t lrow = ((size_t)b * pb.H + h) * pb.S;
-            for (int r = lane; r < kT; r += 32) {
-              const int q = qa + r;
-              const bool in = r < qvalid;
-              const float l = in ? __ldg(P.lse + lrow + q) : 0.f;
-              vec[r] = l * 1.4426950408889634f;
-              vec[kT + r] = in ? __ldg(P.delta + lrow + q) : 0.f;
-            }
-            __syncwarp();
             if (lane == 0) {
-              mbar_arrive_expect_tx(bars.qfull(s), 2 * C::TB);
+              mbar_arrive_expect_tx(bars.qfull(s), 2 * C::TB + C::VEC_BYTES);
               for (int cb = 0; cb < D / 64; ++cb) {
                 tma_load_4d(sbase + C::OFF_Q + s * C::TB + cb * 16384, &mq, bars.qfull(s), cb * 64, h, qa, b);
                 tma_load_4d(sbase + C::OFF_DO + s * C::TB + cb * 16384, &mdo, bars.qfull(s), cb * 64, h, qa, b);
               }
+              bulk_g2s(sbase + C::OFF_VEC + s * C::VEC_BYTES, P.ld2 + ((size_t)b * pb.H + h) * P.Sp + (qa & ~1),
+                       C::VEC_BYTES, bars.qfull(s));
               BRec r;
               r.kind = kRecPair;
               r.flags = full ? 0 : kMasked;
@@ -391,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idSP = idesc_bf16_f32(kT, kT, 0, 0);  // S^T, dP^T: K-major A and B
       constexpr uint32_t idKV = idesc_bf16_f32(kT, D, 0, 1);   // dV, dK: A in TMEM, B MN-major
-      constexpr uint32_t idQ = idesc_bf16_f32(kT, D, 1, 1);    // dQ: A (dS^T smem) and B MN-major
+      // dQ^T (D = 128): A = K^T, B = dS^T; dQ (D = 64): A = dS, B = K; all MN-major
+      constexpr uint32_t idQ = idesc_bf16_f32(D == 128 ? D : kT, D == 128 ? kT : D, 1, 1);
       int rec_n = 0, pair_n = 0, unit_n = 0, dq_n = 0, unit_pairs = 0;
       uint32_t pready_ph = 0;
       bool alive = true, in_unit = false;
@@ -445,26 +444,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the previous unit's dK / dV must have been read out before they are overwritten
         if (first && unit_n > 0 && !mbar_wait(bars.accfree(), (unit_n - 1) & 1, ctl, 55)) break;
         tc_fence_after();
-        // dV += P^T dO ; dK += dS^T Q   (K = 128 queries: columns 0-31 and 64-95 of A / B)
-#pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk) {
-          const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-          mma_ts(tbase + C::TDV, tA + acol, sdesc_sw128(doS + kk * 2048, 16384, 1024), idKV,
-                 (first && kk == 0) ? 0 : 1);
-        }
-#pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk) {
-          const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-          mma_ts(tbase + C::TDK, tB + acol, sdesc_sw128(qS + kk * 2048, 16384, 1024), idKV,
-                 (first && kk == 0) ? 0 : 1);
-        }
-        // dQ_tile = dS K into A (overwrites P^T after the dV MMA read it: in order)
+        // dQ tile into A (S^T there has been consumed by the softmax warpgroups)
         const uint32_t dsS = sbase + C::OFF_DS;
+        if constexpr (D == 128) {
+          // dQ^T = K^T dS^T: TMEM lanes = head dim, columns = queries
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ss(tA, sdesc_sw128(dsS + kk * 2048, 16384, 1024), sdesc_sw128(kS + kk * 2048, 16384, 1024), idQ,
-                 kk > 0);
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ss(tA, sdesc_sw128(kS + kk * 2048, 16384, 1024), sdesc_sw128(dsS + kk * 2048, 16384, 1024), idQ,
+                   kk > 0);
+        } else {
+          // dQ = dS K: TMEM lanes = queries, columns = head dim
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ss(tA, sdesc_sw128(dsS + kk * 2048, 16384, 1024), sdesc_sw128(kS + kk * 2048, 16384, 1024), idQ,
+                   kk > 0);
+        }
         mma_commit(bars.dqfull());
+        // dV += P^T dO ; dK += dS^T Q.  In B the 16 columns of query group kk hold
+        // dS^T (8 columns of bf16 pairs) then P^T (8 columns).
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk) {
+          const uint32_t col = kk * 16 + 8;
+          mma_ts(tbase + C::TDV, tB + col, sdesc_sw128(doS + kk * 2048, 16384, 1024), idKV,
+                 (first && kk == 0) ? 0 : 1);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk) {
+          const uint32_t col = kk * 16;
+          mma_ts(tbase + C::TDK, tB + col, sdesc_sw128(qS + kk * 2048, 16384, 1024), idKV,
+                 (first && kk == 0) ? 0 : 1);
+        }
         mma_commit(bars.qempty(s));
         ++dq_n;
         ++pair_n;
@@ -477,55 +486,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_drain(bars.kvempty(), unit_n & 1, ctl, 56);
     }
     __syncwarp();
-  } else if (warp >= kDqWarp0) {
-    // ------------------------------------------------------------------ dQ accumulation
-    const int q4 = warp & 3;  // TMEM lanes 32*q4 .. (the dQ tile's query rows)
-    const int row = q4 * 32 + lane;
-    const uint32_t tA = tbase + C::TA + ((uint32_t)(q4 * 32) << 16);
-    int rec_n = 0;
-    uint32_t dq_ph = 0;
-    bool alive = true;
-    while (alive) {
-      const int slot = rec_n % kNInfo;
-      alive = __all_sync(0xffffffffu, mbar_wait(bars.infofull(slot), (rec_n / kNInfo) & 1, ctl, 60));
-      if (!alive) break;
-      const BRec r = recs[slot];
-      if (r.kind == kRecStop) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.infoempty(slot));
-        break;
-      }
-      if (r.kind == kRecPair) {
-        alive = __all_sync(0xffffffffu, mbar_wait(bars.dqfull(), dq_ph, ctl, 61));
-        if (!alive) break;
-        dq_ph ^= 1;
-        tc_fence_after();
-        float* dst = P.dq_accum + (((size_t)r.b * pb.S + r.q0 + row) * pb.H + r.h) * D;
-        const bool mine = row < r.qvalid;
-        constexpr int HD = D / 2;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t v[HD];
-#pragma unroll
-          for (int cq = 0; cq < HD / 32; ++cq) tmem_ld32(tA + hh * HD + cq * 32, v + cq * 32);
-#pragma unroll
-          for (int cq = 0; cq < HD / 32; ++cq) tmem_ld_wait(v + cq * 32);
-          if (hh == 1) {  // the whole tile is in registers: release tensor memory
-            tc_fence_before();
-            mbar_arrive(bars.dqfree());
-          }
-          if (mine) {
-#pragma unroll
-            for (int x = 0; x < HD; x += 4)
-              red_add_v4(dst + hh * HD + x, __uint_as_float(v[x]), __uint_as_float(v[x + 1]),
-                         __uint_as_float(v[x + 2]), __uint_as_float(v[x + 3]));
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.infoempty(slot));
-      ++rec_n;
-    }
   } else {
     // ------------------------------------------------------------------ P / dS warpgroups
     const int wg = warp >> 2;              // query columns 64*wg .. +63
@@ -535,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tA = tbase + C::TA + lane_off, tB = tbase + C::TBc + lane_off;
     const float sl2 = P.scale_log2;
     int rec_n = 0, pair_n = 0, unit_pairs = 0;
-    uint32_t sp_ph = 0, acc_ph = 0;
+    uint32_t sp_ph = 0, acc_ph = 0, dq_ph = 0;
     bool alive = true;
     uint8_t* dsT = sm + C::OFF_DS + wg * 16384;  // this warpgroup's 64-query block of dS^T
     while (alive) {
@@ -550,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (r.kind == kRecPair) {
         const int s = pair_n % C::QST;
-        const float* vec = reinterpret_cast<const float*>(sm + C::OFF_VEC + s * C::VEC_BYTES);
+        // (lse2, delta) of query column c is vec[c]; the copy started at an even row
+        const float2* vec = reinterpret_cast<const float2*>(sm + C::OFF_VEC + s * C::VEC_BYTES) + (r.q0 & 1);
         const int* qsegp = pb.seg ? pb.seg + (size_t)r.b * pb.S : nullptr;
         alive = __all_sync(0xffffffffu, mbar_wait(bars.spfull(), sp_ph, ctl, 71));
         if (!alive) break;
@@ -561,22 +522,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cb = pb.causal;
         const int kblk = cb > 0 ? kpos / cb : 0;
         const int kseg = (pb.seg && kr < r.kvalid) ? __ldg(pb.seg + (size_t)r.b * pb.S + kpos) : 0;
+        // this warpgroup's 64 query columns in quarters of 16: S^T from A, dP^T from B;
+        // each quarter's 16 B columns become 8 columns of dS^T then 8 of P^T (bf16 pairs)
+        uint32_t sv[16], dp[16];
+        tmem_ld16(tA + wg * 64, sv);
+        tmem_ld16(tB + wg * 64, dp);
+        tmem_ld_wait16(sv);
+        tmem_ld_wait16(dp);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int c0 = wg * 64 + half * 32;  // first query column of this chunk
-          uint32_t sv[32], dp[32];
-          tmem_ld32(tA + c0, sv);
-          tmem_ld32(tB + c0, dp);
-          tmem_ld_wait(sv);
-          tmem_ld_wait(dp);
-          uint32_t pk[16], dk[16];
+        for (int qq = 0; qq < 4; ++qq) {
+          const int c0 = wg * 64 + qq * 16;
+          uint32_t pk[8], dk[8];
 #pragma unroll
-          for (int x = 0; x < 32; x += 2) {
+          for (int x = 0; x < 16; x += 2) {
             float pp[2], dd[2];
 #pragma unroll
             for (int y = 0; y < 2; ++y) {
               const int cc = c0 + x + y;
-              float p = ex2_approx(fmaf(__uint_as_float(sv[x + y]), sl2, -vec[cc]));
+              const float2 v2 = vec[cc];
+              float p = ex2_approx(fmaf(__uint_as_float(sv[x + y]), sl2, -v2.x));
               if (masked) {
                 const int qpos = r.q0 + cc;
                 bool vis = (kr < r.kvalid) && (cc < r.qvalid);
@@ -585,26 +549,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!vis) p = 0.f;
               }
               pp[y] = p;
-              dd[y] = p * (__uint_as_float(dp[x + y]) - vec[kT + cc]);
+              dd[y] = p * (__uint_as_float(dp[x + y]) - v2.y);
             }
             pk[x / 2] = pack_bf16x2(pp[0], pp[1]);
             dk[x / 2] = pack_bf16x2(dd[0], dd[1]);
           }
-          // P^T and dS^T (bf16 pairs) over the columns this chunk came from
-          tmem_st16(tA + wg * 64 + half * 16, pk);
-          tmem_st16(tB + wg * 64 + half * 16, dk);
-          // dS^T into smem: row kr, queries c0..c0+31 of this block (128B swizzle)
+          if (qq < 3) {  // next quarter's loads fly while this one is stored
+            tmem_ld16(tA + c0 + 16, sv);
+            tmem_ld16(tB + c0 + 16, dp);
+          }
+          tmem_st8(tB + c0, dk);
+          tmem_st8(tB + c0 + 8, pk);
+          // dS^T into smem: row kr, queries c0..c0+15 = 16-byte chunks 2qq, 2qq+1 (128B swizzle)
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            const int chunk = half * 4 + ch;  // 16-byte chunk within the 128-byte row
-            uint4 val = make_uint4(dk[ch * 4], dk[ch * 4 + 1], dk[ch * 4 + 2], dk[ch * 4 + 3]);
-            *reinterpret_cast<uint4*>(dsT + kr * 128 + ((chunk ^ (kr & 7)) * 16)) = val;
+          for (int ch = 0; ch < 2; ++ch) {
+            const int chunk = 2 * qq + ch;
+            *reinterpret_cast<uint4*>(dsT + kr * 128 + ((chunk ^ (kr & 7)) * 16)) =
+                make_uint4(dk[ch * 4], dk[ch * 4 + 1], dk[ch * 4 + 2], dk[ch * 4 + 3]);
+          }
+          if (qq < 3) {
+            tmem_ld_wait16(sv);
+            tmem_ld_wait16(dp);
           }
         }
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bars.pready());
+        // dQ tile (written by the first MMA after pready) -> fp32 accumulator.  Each
+        // warpgroup takes half of the tile's columns; tensor memory is released
+        // before the adds are issued.
+        alive = __all_sync(0xffffffffu, mbar_wait(bars.dqfull(), dq_ph, ctl, 73));
+        if (!alive) break;
+        dq_ph ^= 1;
+        tc_fence_after();
+        if constexpr (D == 128) {
+          // dQ^T: lanes = head-dim index d, columns = queries; a warp-level add covers
+          // 32 consecutive floats of one row
+          uint32_t v[64];
+          tmem_ld32(tA + wg * 64, v);
+          tmem_ld32(tA + wg * 64 + 32, v + 32);
+          tmem_ld_wait(v);
+          tmem_ld_wait(v + 32);
+          tc_fence_before();
+          mbar_arrive(bars.dqfree());
+          float* base = P.dq_accum + (((size_t)r.b * pb.S + r.q0 + wg * 64) * pb.H + r.h) * D + kr;
+          const size_t qstride = (size_t)pb.H * D;
+          const int nq = r.qvalid - wg * 64;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i < nq) red_add_f32(base + (size_t)i * qstride, __uint_as_float(v[i]));
+        } else {
+          // dQ: lanes = query rows, columns = head dim (32 per warpgroup); 16-byte adds
+          uint32_t v[32];
+          tmem_ld32(tA + wg * 32, v);
+          tmem_ld_wait(v);
+          tc_fence_before();
+          mbar_arrive(bars.dqfree());
+          if (kr < r.qvalid) {
+            float* dst = P.dq_accum + (((size_t)r.b * pb.S + r.q0 + kr) * pb.H + r.h) * D + wg * 32;
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+              red_add_v4(dst + x, __uint_as_float(v[x]), __uint_as_float(v[x + 1]), __uint_as_float(v[x + 2]),
+                         __uint_as_float(v[x + 3]));
+          }
+        }
         ++pair_n;
         ++unit_pairs;
       } else if (r.kind == kRecUnitEnd) {
@@ -666,16 +675,16 @@ static cudaError_t launch_bwd_bf16_d(const BwdArgs& a, const Ctx& c, uint64_t* l
     return cudaSuccess;
   }
   const long long rows = (long long)p.B * p.S * p.H;
-  bwd_pre_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, c.stream>>>(p, (const __nv_bfloat16*)a.out,
-                                                                   (const __nv_bfloat16*)a.dout, a.delta,
-                                                                   a.dq_accum);
+  const int Sp = bwd_row_pitch(p.S);
+  bwd_pre_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, c.stream>>>(
+      p, (const __nv_bfloat16*)a.out, (const __nv_bfloat16*)a.dout, a.lse, (float2*)a.delta, Sp, a.dq_accum);
   *launches += 1;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   BwdParams P;
   P.p = p;
-  P.lse = a.lse;
-  P.delta = a.delta;
+  P.ld2 = (const float2*)a.delta;
+  P.Sp = Sp;
   P.dq_accum = a.dq_accum;
   P.dk = (__nv_bfloat16*)a.dk;
   P.dv = (__nv_bfloat16*)a.dv;

@@ -7,7 +7,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/ra.h"
+#include "ra.h"
 #include "ra_internal.h"
 
 #define RA_API extern "C" __attribute__((visibility("default")))

@@ -37,7 +37,7 @@ struct BwdArgs {
   void* dk;
   void* dv;
   float* dq_accum;  // [B, S, H, D] fp32 scratch (bf16 path)
-  float* delta;     // [B, H, S]   fp32 scratch
+  float* delta;     // fp32 path: [B, H, S] Delta; bf16 path: float2 (lse*log2(e), Delta) rows of bwd_row_pitch
 };
 
 // Launch context: device facts and the device status word.
@@ -57,13 +57,19 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const Ctx& c, uint64_t* launches, 
 cudaError_t launch_bwd_bf16(const BwdArgs& a, const Ctx& c, uint64_t* launches, const char** why);
 cudaError_t launch_selftest_timeout(const Ctx& c, uint64_t* launches);
 
-// Scratch layout of the bf16 backward (byte offsets into the caller's workspace).
+// Scratch layout of the bf16 backward (byte offsets into the caller's workspace):
+// the fp32 dQ accumulator, then (lse*log2(e), Delta) float2 pairs per (b, h) row
+// with an even row pitch (16-byte aligned pairs of entries) and a tail pad so
+// that a 130-entry bulk copy starting at any even index stays inside.
+constexpr int kBwdVecEntries = 130;
+inline int bwd_row_pitch(int S) { return S + (S & 1); }
 inline size_t bwd_delta_offset(int B, int S, int H, int D) {
   size_t dq = (size_t)B * S * H * D * sizeof(float);
   return (dq + 255) & ~(size_t)255;
 }
 inline size_t bwd_workspace_bytes(int B, int S, int H, int D) {
-  return bwd_delta_offset(B, S, H, D) + (((size_t)B * H * S * sizeof(float) + 255) & ~(size_t)255);
+  const size_t vec = ((size_t)B * H * bwd_row_pitch(S) + kBwdVecEntries) * 2 * sizeof(float);
+  return bwd_delta_offset(B, S, H, D) + ((vec + 255) & ~(size_t)255);
 }
 
 }  // namespace ra
