@@ -170,11 +170,12 @@ __global__ void bwd_fin_kernel(size_t n4, const float4* __restrict__ acc, uint2*
   }
 }
 
-// Unit u -> (b, h, key shard k, tile t).  Ordered by increasing key position
-// (largest causal work first), heads and batches interleaved.
+// Unit u -> (b, h, key shard k, tile t).  Head-major, so the head's Q, dO and
+// fp32 dQ accumulator stay resident in L2 while its key tiles are processed;
+// within a head key tiles go by increasing position (longest causal work first).
 __device__ __forceinline__ void bunit_coords(const BwdParams& P, int u, int& b, int& h, int& k, int& t) {
-  const int BH = P.p.B * P.p.H;
-  const int rank = u / BH, bh = u % BH;
+  const int per_head = P.p.N * P.tiles_per_shard;
+  const int bh = u / per_head, rank = u % per_head;
   k = rank / P.tiles_per_shard;
   t = rank % P.tiles_per_shard;
   b = bh / P.p.H;
@@ -532,27 +533,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
           const int c0 = wg * 64 + qq * 16;
+          // branch-free exponentials for the whole quarter (one basic block, so the
+          // independent per-element chains interleave), then the mask, then dS
+          float pq[16], dq16[16];
+#pragma unroll
+          for (int y = 0; y < 16; ++y) {
+            const float2 v2 = vec[c0 + y];
+            pq[y] = ex2_approx(fmaf(__uint_as_float(sv[y]), sl2, -v2.x));
+            dq16[y] = __uint_as_float(dp[y]) - v2.y;
+          }
+          if (masked) {  // one uniform branch around the whole quarter; selects inside
+#pragma unroll
+            for (int y = 0; y < 16; ++y) {
+              const int cc = c0 + y;
+              const int qpos = r.q0 + cc;
+              bool vis = (kr < r.kvalid) & (cc < r.qvalid);
+              vis &= (cb <= 0) | (qpos / max(cb, 1) >= kblk);
+              const int qs = qsegp ? __ldg(qsegp + min(qpos, pb.S - 1)) : kseg;
+              vis &= (qs == kseg);
+              pq[y] = vis ? pq[y] : 0.f;
+            }
+          }
           uint32_t pk[8], dk[8];
 #pragma unroll
-          for (int x = 0; x < 16; x += 2) {
-            float pp[2], dd[2];
-#pragma unroll
-            for (int y = 0; y < 2; ++y) {
-              const int cc = c0 + x + y;
-              const float2 v2 = vec[cc];
-              float p = ex2_approx(fmaf(__uint_as_float(sv[x + y]), sl2, -v2.x));
-              if (masked) {
-                const int qpos = r.q0 + cc;
-                bool vis = (kr < r.kvalid) && (cc < r.qvalid);
-                if (cb > 0) vis = vis && (qpos / cb >= kblk);
-                if (qsegp) vis = vis && (__ldg(qsegp + min(qpos, pb.S - 1)) == kseg);
-                if (!vis) p = 0.f;
-              }
-              pp[y] = p;
-              dd[y] = p * (__uint_as_float(dp[x + y]) - v2.y);
-            }
-            pk[x / 2] = pack_bf16x2(pp[0], pp[1]);
-            dk[x / 2] = pack_bf16x2(dd[0], dd[1]);
+          for (int x = 0; x < 8; ++x) {
+            pk[x] = pack_bf16x2(pq[2 * x], pq[2 * x + 1]);
+            dk[x] = pack_bf16x2(pq[2 * x] * dq16[2 * x], pq[2 * x + 1] * dq16[2 * x + 1]);
           }
           if (qq < 3) {  // next quarter's loads fly while this one is stored
             tmem_ld16(tA + c0 + 16, sv);

@@ -107,14 +107,15 @@ struct FwdParams {
 
 __device__ __forceinline__ int floordiv_pos(int a, int c) { return a / c; }  // a >= 0
 
-// Unit u -> (b, h, query shard j, pair index).  Units are ordered by
-// decreasing global query position (longest causal work first), heads and
-// batches interleaved; CTA c takes units c, c + G, c + 2G, ...
+// Unit u -> (b, h, query shard j, pair index).  Units are head-major: all CTAs
+// work on one or two heads at a time, so that head's K and V stay resident in
+// L2 while every query tile of the head streams over them.  Within a head the
+// query tiles go by decreasing position (longest causal work first); CTA c
+// takes units c, c + G, c + 2G, ...
 __device__ __forceinline__ void unit_coords(const FwdParams& P, int u, int& b, int& h, int& j, int& pr) {
-  const int BH = P.p.B * P.p.H;
-  const int rank = u / BH;
-  const int bh = u % BH;
-  const int g = P.p.N * P.pairs_per_shard - 1 - rank;
+  const int per_head = P.p.N * P.pairs_per_shard;
+  const int bh = u / per_head;
+  const int g = per_head - 1 - (u % per_head);
   j = g / P.pairs_per_shard;
   pr = g % P.pairs_per_shard;
   b = bh / P.p.H;
