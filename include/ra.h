@@ -128,6 +128,40 @@ uint64_t ra_kernel_launches(void);
  */
 ra_status ra_selftest_timeout(int64_t limit_ns, void* stream);
 
+/*
+ * Size in bytes of the built-in scratch array used by ra_bwd_noalloc (64 MiB).
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory.
+ */
+#define RA_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * Backward without a caller workspace, for callers that cannot allocate device
+ * memory (no cudaMalloc where they run: fixed arenas, runtimes that forbid
+ * allocation after start-up, code that must not synchronize the device).  Same
+ * arguments, results and rules as ra_bwd, minus the workspace: the scratch is
+ * a RA_NOALLOC_SCRATCH_BYTES array in the library's device image, held by
+ * every GPU that uses this call until the process exits.  This function calls
+ * no cudaMalloc, cudaFree or other allocating routine.
+ *   - Problems whose ra_bwd_workspace_size(...) exceeds the array are
+ *     rejected with RA_ERR_INVALID_ARG (use ra_bwd instead).
+ *   - The first call on a device looks up the array's device address (once,
+ *     with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents (the part that must start at zero is cleared by every call).
+ *     Calls that overlap on the GPU (unordered streams) race on it.
+ */
+ra_status ra_bwd_noalloc(const void* q, const void* k, const void* v,
+                         const void* out, const float* lse, const void* dout,
+                         const int32_t* segment_ids, int causal_block_size,
+                         int num_shards, int query_chunk_size, int key_chunk_size,
+                         int batch, int seq, int heads, int head_dim, ra_dtype dtype,
+                         void* dq, void* dk, void* dv, void* stream);
+
+/* RA_NOALLOC_SCRATCH_BYTES, as built into the library. */
+size_t ra_bwd_noalloc_max_scratch(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -116,6 +116,10 @@ ra_status validate(const void* const* ptrs, const char* const* names, int nptr,
 }
 
 }  // namespace
+
+// Record a message for ra_last_error() on behalf of entry points in other files.
+ra_status set_last_error(ra_status s, const char* msg) { return fail(s, "%s", msg); }
+
 }  // namespace ra
 
 using namespace ra;

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "ra.h"
+
 namespace ra {
 
 // One attention problem: [B, S, H, D] tensors split into N contiguous virtual shards.
@@ -56,6 +58,9 @@ cudaError_t launch_bwd_f32(const BwdArgs& a, const Ctx& c, uint64_t* launches);
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const Ctx& c, uint64_t* launches, const char** why);
 cudaError_t launch_bwd_bf16(const BwdArgs& a, const Ctx& c, uint64_t* launches, const char** why);
 cudaError_t launch_selftest_timeout(const Ctx& c, uint64_t* launches);
+
+// Sets the calling thread's ra_last_error() message and returns s.
+ra_status set_last_error(ra_status s, const char* msg);
 
 // Scratch layout of the bf16 backward (byte offsets into the caller's workspace):
 // the fp32 dQ accumulator, then (lse*log2(e), Delta) float2 pairs per (b, h) row

@@ -20,7 +20,7 @@ RA_F32, RA_BF16 = 0, 1
 _STATUS = {1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "device wait timed out"}
 
 EXPORTS = ("ra_fwd", "ra_bwd", "ra_bwd_workspace_size", "ra_sync_check", "ra_last_error",
-           "ra_kernel_launches", "ra_selftest_timeout")
+           "ra_kernel_launches", "ra_selftest_timeout", "ra_bwd_noalloc", "ra_bwd_noalloc_max_scratch")
 
 
 class RAError(RuntimeError):
@@ -56,6 +56,11 @@ def lib() -> ctypes.CDLL:
     L.ra_kernel_launches.argtypes = []
     L.ra_selftest_timeout.restype = i32
     L.ra_selftest_timeout.argtypes = [ctypes.c_int64, vp]
+    L.ra_bwd_noalloc.restype = i32
+    L.ra_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                 vp, vp, vp, vp]
+    L.ra_bwd_noalloc_max_scratch.restype = sz
+    L.ra_bwd_noalloc_max_scratch.argtypes = []
     _lib = L
     return L
 
@@ -151,6 +156,26 @@ def bwd(q, k, v, out, lse, dout, segment_ids=None, causal_block_size=0, num_shar
                         int(causal_block_size), int(num_shards), int(qc), int(kc), B, S, H, D,
                         _dtype_code(q), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
                         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dq, dk, dv
+
+
+def bwd_noalloc(q, k, v, out, lse, dout, segment_ids=None, causal_block_size=0, num_shards=1,
+                query_chunk_size=None, key_chunk_size=None, dq=None, dk=None, dv=None, stream=None):
+    """ra_bwd_noalloc: the backward with the library's built-in scratch (for callers
+    that cannot allocate device memory).  Returns (dq, dk, dv)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _check_tensor(name, t, q)
+    _check_tensor("lse", lse, dtype=torch.float32)
+    B, S, H, D = q.shape
+    if segment_ids is not None:
+        _check_tensor("segment_ids", segment_ids, dtype=torch.int32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    qc, kc = _chunks(S, num_shards, query_chunk_size, key_chunk_size)
+    _check(lib().ra_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(segment_ids),
+                                int(causal_block_size), int(num_shards), int(qc), int(kc), B, S, H, D,
+                                _dtype_code(q), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
     return dq, dk, dv
 
 
