@@ -396,6 +396,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pready_ph = 0;
       bool alive = true, in_unit = false;
       const uint32_t tA = tbase + C::TA, tB = tbase + C::TBc;
+      // Shared-memory descriptors built once; each MMA adds a compile-time byte offset.
+      const uint64_t kdK = sdesc_sw128(sbase + C::OFF_K, 16, 1024);     // K, K-major
+      const uint64_t kdV = sdesc_sw128(sbase + C::OFF_V, 16, 1024);     // V, K-major
+      const uint64_t kdQ = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);     // Q stage 0, K-major
+      const uint64_t kdO = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);    // dO stage 0, K-major
+      const uint64_t mdK = sdesc_sw128(sbase + C::OFF_K, 16384, 1024);  // K, MN-major
+      const uint64_t mdQ = sdesc_sw128(sbase + C::OFF_Q, 16384, 1024);  // Q stage 0, MN-major
+      const uint64_t mdO = sdesc_sw128(sbase + C::OFF_DO, 16384, 1024); // dO stage 0, MN-major
+      const uint64_t mdS = sdesc_sw128(sbase + C::OFF_DS, 16384, 1024); // dS^T, MN-major
       while (alive) {
         const int slot = rec_n % kNInfo;
         if (!mbar_wait(bars.infofull(slot), (rec_n / kNInfo) & 1, ctl, 50)) break;
@@ -422,13 +431,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = pair_n % C::QST;
         if (!mbar_wait(bars.qfull(s), (pair_n / C::QST) & 1, ctl, 52)) break;
         tc_fence_after();
-        const uint32_t kS = sbase + C::OFF_K, vS = sbase + C::OFF_V;
-        const uint32_t qS = sbase + C::OFF_Q + s * C::TB, doS = sbase + C::OFF_DO + s * C::TB;
         // dP^T = V dO^T into B (B was last read by the previous pair's dK MMA: in order)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tB, sdesc_sw128(vS + off, 16, 1024), sdesc_sw128(doS + off, 16, 1024), idSP, kk > 0);
+          mma_ss(tB, sdesc_add(kdV, off), sdesc_add(kdO, s * C::TB + off), idSP, kk > 0);
         }
         // S^T = K Q^T into A, once the previous dQ tile has been read out of A
         if (dq_n > 0 && !mbar_wait(bars.dqfree(), (dq_n - 1) & 1, ctl, 53)) break;
@@ -436,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tA, sdesc_sw128(kS + off, 16, 1024), sdesc_sw128(qS + off, 16, 1024), idSP, kk > 0);
+          mma_ss(tA, sdesc_add(kdK, off), sdesc_add(kdQ, s * C::TB + off), idSP, kk > 0);
         }
         mma_commit(bars.spfull());
         // wait for P^T, dS^T (TMEM) and dS^T (smem)
@@ -446,18 +453,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (first && unit_n > 0 && !mbar_wait(bars.accfree(), (unit_n - 1) & 1, ctl, 55)) break;
         tc_fence_after();
         // dQ tile into A (S^T there has been consumed by the softmax warpgroups)
-        const uint32_t dsS = sbase + C::OFF_DS;
         if constexpr (D == 128) {
           // dQ^T = K^T dS^T: TMEM lanes = head dim, columns = queries
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ss(tA, sdesc_sw128(kS + kk * 2048, 16384, 1024), sdesc_sw128(dsS + kk * 2048, 16384, 1024), idQ,
+            mma_ss(tA, sdesc_add(mdK, kk * 2048), sdesc_add(mdS, kk * 2048), idQ,
                    kk > 0);
         } else {
           // dQ = dS K: TMEM lanes = queries, columns = head dim
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ss(tA, sdesc_sw128(dsS + kk * 2048, 16384, 1024), sdesc_sw128(kS + kk * 2048, 16384, 1024), idQ,
+            mma_ss(tA, sdesc_add(mdS, kk * 2048), sdesc_add(mdK, kk * 2048), idQ,
                    kk > 0);
         }
         mma_commit(bars.dqfull());
@@ -466,13 +472,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk) {
           const uint32_t col = kk * 16 + 8;
-          mma_ts(tbase + C::TDV, tB + col, sdesc_sw128(doS + kk * 2048, 16384, 1024), idKV,
+          mma_ts(tbase + C::TDV, tB + col, sdesc_add(mdO, s * C::TB + kk * 2048), idKV,
                  (first && kk == 0) ? 0 : 1);
         }
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk) {
           const uint32_t col = kk * 16;
-          mma_ts(tbase + C::TDK, tB + col, sdesc_sw128(qS + kk * 2048, 16384, 1024), idKV,
+          mma_ts(tbase + C::TDK, tB + col, sdesc_add(mdQ, s * C::TB + kk * 2048), idKV,
                  (first && kk == 0) ? 0 : 1);
         }
         mma_commit(bars.qempty(s));

@@ -123,7 +123,7 @@ __device__ __forceinline__ void unit_coords(const FwdParams& P, int u, int& b, i
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-partitions -> <= 168 registers
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const FwdParams P) {
   using C = Cfg<D>;
@@ -354,45 +354,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 0, 1);
-      int rec_n = 0, tile_n = 0, unit_n = 0;
+      int tile_n = 0, unit_n = 0;
       uint32_t ofree_ph[2] = {1, 1}, pready_ph[2] = {0, 0};
       bool alive = true;
-      auto take = [&](Rec& r) -> bool {
-        const int slot = rec_n % kNInfo;
-        if (!mbar_wait(bars.infofull(slot), (rec_n / kNInfo) & 1, ctl, 20)) return false;
-        r = recs[slot];
-        return true;
+      // Shared-memory descriptors of every operand buffer, built once; each MMA
+      // adds a compile-time byte offset.
+      const uint64_t dQ0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(sbase + C::OFF_V, 16384, 1024);
+      auto dQ = [&](int w) { return sdesc_add(dQ0, w * C::QT); };
+      auto dK = [&](int s) { return sdesc_add(dK0, s * C::KVT); };
+      auto dV = [&](int s) { return sdesc_add(dV0, s * C::KVT); };
+      struct MRec {  // the two record fields the MMA warp needs
+        int kind, flags;
       };
       auto release = [&](int n) { mbar_arrive(bars.infoempty(n % kNInfo)); };
-      auto issue_S = [&](const Rec& r, int stage) -> bool {
+      auto issue_S = [&](const MRec& r, int stage) -> bool {
         if (!mbar_wait(bars.kfull(stage), (tile_n / C::KST) & 1, ctl, 21)) return false;
         tc_fence_after();
         for (int w = 0; w < 2; ++w) {
           if (r.flags & (w == 0 ? kSkip0 : kSkip1)) continue;
-          const uint32_t qa = sbase + C::OFF_Q + w * C::QT;
-          const uint32_t ka = sbase + C::OFF_K + stage * C::KVT;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tbase + w * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS,
-                   kk > 0);
+            mma_ss(tbase + w * 128, sdesc_add(dQ(w), off), sdesc_add(dK(stage), off), idS, kk > 0);
           }
           mma_commit(bars.sfull(w));
         }
         mma_commit(bars.kempty(stage));
         return true;
       };
-      Rec rec, nxt;
-      alive = take(rec);
+      // Record i of the ring: wait until published, read its kind and flags.
+      auto take_at = [&](MRec& r, int i) -> bool {
+        if (!mbar_wait(bars.infofull(i % kNInfo), (i / kNInfo) & 1, ctl, 20)) return false;
+        const int2 kf = *reinterpret_cast<const int2*>(&recs[i % kNInfo]);
+        r.kind = kf.x;
+        r.flags = kf.y;
+        return true;
+      };
+      MRec rec, nxt;
+      int rec_i = 0;
+      alive = take_at(rec, rec_i);
       while (alive && rec.kind != kRecStop) {
-        // rec is the first tile of a unit
+        // rec is the first record of a unit
         alive = mbar_wait(bars.qfull(), unit_n & 1, ctl, 22);
         if (alive && rec.kind == kRecUnitEnd) {  // a unit without visible tiles
           mma_commit(bars.qempty());
-          release(rec_n);
-          ++rec_n;
+          release(rec_i);
+          ++rec_i;
           ++unit_n;
-          alive = take(rec);
+          alive = take_at(rec, rec_i);
           continue;
         }
         int stage = tile_n % C::KST;
@@ -400,10 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool first[2] = {true, true};
         bool any_pv[2] = {false, false};
         while (alive) {
-          ++rec_n;
-          alive = take(nxt);
-          if (!alive) break;
-          // PV for rec, interleaved with S for nxt
+          // rec: tile t (record rec_i); nxt: record t + 1 (a tile or the unit end).
+          // Order on the tensor pipe: PV0(t), S0(t+1), PV1(t), S1(t+1).
+          const int nxt_i = rec_i + 1;
+          if (!take_at(nxt, nxt_i)) { alive = false; break; }
           if (!mbar_wait(bars.vfull(stage), (tile_n / C::KST) & 1, ctl, 23)) { alive = false; break; }
           const int nstage = (tile_n + 1) % C::KST;
           bool nxt_k_ready = false;
@@ -416,11 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!mbar_wait(bars.pready(w), pready_ph[w], ctl, 25)) { alive = false; break; }
               pready_ph[w] ^= 1;
               tc_fence_after();
-              const uint32_t va = sbase + C::OFF_V + stage * C::KVT;
 #pragma unroll
               for (int kk = 0; kk < kBN / 16; ++kk)
-                mma_ts(tbase + C::TCOL_O + w * D, tbase + w * 128 + kk * 8,
-                       sdesc_sw128(va + kk * 2048, 16384, 1024), idO, first[w] ? (kk > 0) : 1);
+                mma_ts(tbase + C::TCOL_O + w * D, tbase + w * 128 + kk * 8, sdesc_add(dV(stage), kk * 2048), idO,
+                       first[w] ? (kk > 0) : 1);
               first[w] = false;
               any_pv[w] = true;
             }
@@ -430,13 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 nxt_k_ready = true;
               }
-              const uint32_t qa = sbase + C::OFF_Q + w * C::QT;
-              const uint32_t ka = sbase + C::OFF_K + nstage * C::KVT;
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_ss(tbase + w * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS,
-                       kk > 0);
+                mma_ss(tbase + w * 128, sdesc_add(dQ(w), off), sdesc_add(dK(nstage), off), idS, kk > 0);
               }
               mma_commit(bars.sfull(w));
             }
@@ -444,24 +451,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!alive) break;
           mma_commit(bars.vempty(stage));
           if (nxt.kind == kRecTile) mma_commit(bars.kempty(nstage));
-          release(rec_n - 1);
+          release(rec_i);
           ++tile_n;
           stage = nstage;
           if (nxt.kind != kRecTile) {  // unit end
             for (int w = 0; w < 2; ++w)
               if (any_pv[w]) mma_commit(bars.odone(w));
             mma_commit(bars.qempty());
-            release(rec_n);
-            ++rec_n;
+            release(nxt_i);
+            rec_i = nxt_i + 1;
             ++unit_n;
             break;
           }
           rec = nxt;
+          rec_i = nxt_i;
         }
         if (!alive) break;
-        alive = take(rec);
+        alive = take_at(rec, rec_i);
       }
-      if (alive && rec.kind == kRecStop) release(rec_n);
+      if (alive && rec.kind == kRecStop) release(rec_i);
       // Drain: wait for every MMA issued by this thread before TMEM is freed.
       mma_commit(bars.qempty());
       mbar_drain(bars.qempty(), (unit_n & 1), ctl, 27);
@@ -541,18 +549,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_use = m_tile;
         }
         const float mb = (m_use == -INFINITY) ? 0.f : m_use;
-        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};  // two packed accumulators
         uint32_t pk[64];
 #pragma unroll
         for (int x = 0; x < 64; ++x) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * x]), sl2, -mb));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * x + 1]), sl2, -mb));
-          rs4[x & 3] += p0 + p1;
+          float a0, a1;
+          fma_f32x2(a0, a1, __uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1]), sl2, sl2, -mb, -mb);
+          const float p0 = ex2_approx(a0);
+          const float p1 = ex2_approx(a1);
+          const int acc = (x & 1) * 2;
+          add_f32x2(rs[acc], rs[acc + 1], rs[acc], rs[acc + 1], p0, p1);
           pk[x] = pack_bf16x2(p0, p1);
           if (x == 31) tmem_st32(tS, pk);  // first half of P goes out while the rest is computed
         }
         tmem_st32(tS + 32, pk + 32);
-        l = l * corr + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+        l = l * corr + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
         if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
           for (int cq = 0; cq < D / 32; ++cq) {
