@@ -543,10 +543,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // independent per-element chains interleave), then the mask, then dS
           float pq[16], dq16[16];
 #pragma unroll
-          for (int y = 0; y < 16; ++y) {
-            const float2 v2 = vec[c0 + y];
-            pq[y] = ex2_approx(fmaf(__uint_as_float(sv[y]), sl2, -v2.x));
-            dq16[y] = __uint_as_float(dp[y]) - v2.y;
+          for (int y = 0; y < 16; y += 2) {
+            const float2 va = vec[c0 + y], vb = vec[c0 + y + 1];
+            float a0, a1;
+            fma_f32x2(a0, a1, __uint_as_float(sv[y]), __uint_as_float(sv[y + 1]), sl2, sl2, -va.x, -vb.x);
+            pq[y] = ex2_approx(a0);
+            pq[y + 1] = ex2_approx(a1);
+            add_f32x2(dq16[y], dq16[y + 1], __uint_as_float(dp[y]), __uint_as_float(dp[y + 1]), -va.y, -vb.y);
           }
           if (masked) {  // one uniform branch around the whole quarter; selects inside
 #pragma unroll
@@ -564,7 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int x = 0; x < 8; ++x) {
             pk[x] = pack_bf16x2(pq[2 * x], pq[2 * x + 1]);
-            dk[x] = pack_bf16x2(pq[2 * x] * dq16[2 * x], pq[2 * x + 1] * dq16[2 * x + 1]);
+            float d0, d1;
+            mul_f32x2(d0, d1, pq[2 * x], pq[2 * x + 1], dq16[2 * x], dq16[2 * x + 1]);
+            dk[x] = pack_bf16x2(d0, d1);
           }
           if (qq < 3) {  // next quarter's loads fly while this one is stored
             tmem_ld16(tA + c0 + 16, sv);
