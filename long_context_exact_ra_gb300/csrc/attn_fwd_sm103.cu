@@ -191,7 +191,19 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
       ++rec_n;
       return true;
     };
-    for (int u = blockIdx.x; u < P.num_units && alive; u += gridDim.x) {
+    // Units go out in balanced pairs: within a head, unit r (long causal work)
+    // with unit per_head - 1 - r (short), so every CTA's step takes about the same
+    // time and all CTAs move through one or two heads together, keeping those
+    // heads' operands resident in L2.
+    const int per_head = pb.N * P.pairs_per_shard;
+    const int pairs_per_head = (per_head + 1) / 2;
+    const int num_super = (P.num_units / per_head) * pairs_per_head;
+    for (int su = blockIdx.x; su < num_super && alive; su += gridDim.x)
+     for (int half = 0; half < 2 && alive; ++half) {
+      const int rr = su % pairs_per_head;
+      const int rank = half == 0 ? rr : per_head - 1 - rr;
+      if (half == 1 && rank == rr) continue;  // odd count: the middle unit has no partner
+      const int u = (su / pairs_per_head) * per_head + rank;
       int b, h, j, pr;
       unit_coords(P, u, b, h, j, pr);
       const int shard0 = j * pb.Ssh;
@@ -685,7 +697,9 @@ static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* l
     if (e != cudaSuccess) return e;
     attr_set[c.device][di] = true;
   }
-  const int grid = std::min(c.num_sms, P.num_units);
+  const int per_head = p.N * P.pairs_per_shard;
+  const int num_super = (P.num_units / per_head) * ((per_head + 1) / 2);  // balanced unit pairs
+  const int grid = std::min(c.num_sms, num_super);
   fwd_bf16_kernel<D><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, P);
   *launches += 1;
   return cudaGetLastError();
