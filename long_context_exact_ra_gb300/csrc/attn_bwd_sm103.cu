@@ -112,8 +112,8 @@ struct BwdParams {
   float scale_log2;  // log2(e) / sqrt(D)
 };
 
-__device__ __forceinline__ void red_add_f32(float* addr, float a) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+__device__ __forceinline__ void red_add_v2(float* addr, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "f"(a), "f"(b) : "memory");
 }
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
@@ -613,8 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         dq_ph ^= 1;
         tc_fence_after();
         if constexpr (D == 128) {
-          // dQ^T: lanes = head-dim index d, columns = queries; a warp-level add covers
-          // 32 consecutive floats of one row
+          // dQ^T: lanes = head-dim index d, columns = queries.  Neighbouring lanes
+          // (d even, d + 1) swap one value per query pair so that the even lane adds
+          // (d, d + 1) of query i and the odd lane (d - 1, d) of query i + 1: one
+          // 8-byte add per lane, and a warp-level add covers 128 bytes of two rows.
           uint32_t v[64];
           tmem_ld32(tA + wg * 64, v);
           tmem_ld32(tA + wg * 64 + 32, v + 32);
@@ -622,12 +624,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait(v + 32);
           tc_fence_before();
           mbar_arrive(bars.dqfree());
-          float* base = P.dq_accum + (((size_t)r.b * pb.S + r.q0 + wg * 64) * pb.H + r.h) * D + kr;
           const size_t qstride = (size_t)pb.H * D;
-          const int nq = r.qvalid - wg * 64;
+          const int odd = lane & 1;
+          // even lane: row i, columns d, d + 1; odd lane: row i + 1, columns d - 1, d
+          float* base = P.dq_accum + (((size_t)r.b * pb.S + r.q0 + wg * 64) * pb.H + r.h) * D + kr - odd +
+                        odd * qstride;
+          const int nq = r.qvalid - wg * 64 - odd;
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (i < nq) red_add_f32(base + (size_t)i * qstride, __uint_as_float(v[i]));
+          for (int i = 0; i < 64; i += 2) {
+            const float lo = __uint_as_float(v[i]), hi = __uint_as_float(v[i + 1]);
+            const float got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+            if (i < nq) red_add_v2(base + (size_t)i * qstride, odd ? got : lo, odd ? hi : got);
+          }
         } else {
           // dQ: lanes = query rows, columns = head dim (32 per warpgroup); 16-byte adds
           uint32_t v[32];
