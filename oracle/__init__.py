@@ -13,3 +13,10 @@ from .attention import (  # noqa: F401
     ref_ring_fwd,
     visible,
 )
+from .decode import (  # noqa: F401
+    decode_visible,
+    filled_lengths,
+    ref_decode,
+    ref_decode_rows,
+    ref_ring_decode,
+)
