@@ -107,6 +107,52 @@ ra_status ra_bwd(const void* q, const void* k, const void* v,
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Decoding against a KV cache (the `cache_idx` inference path).
+ *
+ * T = new_tokens query tokens per batch row attend to a key/value cache of
+ * capacity S = cache_len (comparison page "RingAttention与传统注意力机制对比为
+ * 什么它是大语言模型的终极解决方案", §关键参数配置: cache_idx, the inference
+ * cache index; §推理成本显著降低: incremental decoding with a KV cache).
+ *   - New token t of batch row b sits at position cache_idx[b] + t.  Its key
+ *     and value must already be in the cache at that position (the caller
+ *     writes them; this call only reads the cache).
+ *   - The cache holds L_b = clamp(cache_idx[b] + T, 0, S) filled entries;
+ *     entries j >= L_b are not keys.  Key j is visible to token t iff j < L_b,
+ *     the causal block rule (cache_idx[b] + t) / c >= j / c holds (c =
+ *     causal_block_size > 0; a negative position sees nothing) and, with
+ *     segment ids, q_segment_ids[b, t] == kv_segment_ids[b, j].
+ *   - The cache is cut into num_shards contiguous virtual shards.  Each shard
+ *     is reduced to lazy-softmax partials and every token merges the shards in
+ *     ring order k = (j - i) mod N from its home shard j = pos / (S / N)
+ *     (paper review page, 环形注意力算法; code walk-through page §2).
+ * Layouts (row-major, contiguous, device memory):
+ *   q, out                : [batch, new_tokens, heads, head_dim], element type `dtype`
+ *   k_cache, v_cache      : [batch, cache_len, heads, head_dim], element type `dtype`
+ *   cache_idx             : [batch] int32 (device memory, read by the kernels)
+ *   q_segment_ids         : [batch, new_tokens] int32, kv_segment_ids: [batch, cache_len]
+ *                           int32; both or neither (NULL = no segment mask)
+ *   lse                   : [batch, heads, new_tokens] float32, natural log;
+ *                           a token with no visible key gets out = 0, lse = -inf
+ * Supported: dtype RA_BF16 or RA_F32 with head_dim in {64, 128}; 1 <= new_tokens
+ * <= 64 (new_tokens = 0 returns RA_OK at once).  Requirements (else
+ * RA_ERR_INVALID_ARG): batch, heads in [1, 65535], cache_len >= 0,
+ * cache_len % num_shards == 0, causal_block_size >= 0, q, out, lse, cache_idx
+ * non-NULL, k_cache and v_cache non-NULL when cache_len > 0, tensor pointers
+ * 16-byte aligned and int32 pointers 4-byte aligned, workspace of at least
+ * ra_decode_workspace_size(...) bytes (16-byte aligned; NULL allowed when
+ * that size is 0).  Two kernel launches on `stream`, asynchronous.
+ */
+size_t ra_decode_workspace_size(int batch, int new_tokens, int cache_len, int heads, int head_dim,
+                                int num_shards, ra_dtype dtype);
+
+ra_status ra_decode(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* cache_idx, const int32_t* q_segment_ids,
+                    const int32_t* kv_segment_ids, int causal_block_size, int num_shards,
+                    int batch, int new_tokens, int cache_len, int heads, int head_dim,
+                    ra_dtype dtype, void* out, float* lse,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronize `stream`, then read and clear the device status word that the
  * kernels set when a bounded wait runs out.  Returns RA_ERR_TIMEOUT (message
  * names the wait site) if any kernel gave up since the last check,

@@ -208,6 +208,93 @@ RA_API ra_status ra_bwd(const void* q, const void* k, const void* v, const void*
   return ok();
 }
 
+RA_API size_t ra_decode_workspace_size(int batch, int new_tokens, int cache_len, int heads, int head_dim,
+                                       int num_shards, ra_dtype dtype) {
+  (void)dtype;
+  if (batch < 1 || new_tokens < 1 || cache_len < 0 || heads < 1 || head_dim < 1 || num_shards < 1) return 0;
+  return decode_workspace_bytes(batch, new_tokens, cache_len, heads, head_dim, num_shards);
+}
+
+RA_API ra_status ra_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* cache_idx,
+                           const int32_t* q_segment_ids, const int32_t* kv_segment_ids, int causal_block_size,
+                           int num_shards, int batch, int new_tokens, int cache_len, int heads, int head_dim,
+                           ra_dtype dtype, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (batch < 1 || batch > 65535 || heads < 1 || heads > 65535 || new_tokens < 0 || cache_len < 0 ||
+      head_dim < 1)
+    return fail(RA_ERR_INVALID_ARG, "bad shape batch=%d new_tokens=%d cache_len=%d heads=%d head_dim=%d", batch,
+                new_tokens, cache_len, heads, head_dim);
+  if (num_shards < 1) return fail(RA_ERR_INVALID_ARG, "num_shards=%d must be >= 1", num_shards);
+  if (cache_len % num_shards != 0)
+    return fail(RA_ERR_INVALID_ARG, "cache_len=%d not divisible by num_shards=%d", cache_len, num_shards);
+  if (causal_block_size < 0)
+    return fail(RA_ERR_INVALID_ARG, "causal_block_size=%d must be >= 0", causal_block_size);
+  if ((q_segment_ids == nullptr) != (kv_segment_ids == nullptr))
+    return fail(RA_ERR_INVALID_ARG, "q_segment_ids and kv_segment_ids must be given together");
+  if (head_dim != 64 && head_dim != 128)
+    return fail(RA_ERR_UNSUPPORTED, "decode supports head_dim 64 and 128, got %d", head_dim);
+  if (new_tokens > 64) return fail(RA_ERR_UNSUPPORTED, "decode takes at most 64 new tokens, got %d", new_tokens);
+  if (new_tokens == 0) return ok();
+  {
+    const DecodeSplit sp = decode_split(batch, new_tokens, cache_len, heads, num_shards);
+    if ((long long)sp.P * heads * ((new_tokens + 7) / 8) > 0x7fffffffLL)
+      return fail(RA_ERR_INVALID_ARG, "cache too long for one decode launch (%d work items per head)", sp.P);
+  }
+  struct {
+    const void* p;
+    const char* name;
+    bool required;
+    uintptr_t align;
+  } ptrs[] = {{q, "q", true, 16},
+              {k_cache, "k_cache", cache_len > 0, 16},
+              {v_cache, "v_cache", cache_len > 0, 16},
+              {out, "out", true, 16},
+              {lse, "lse", true, 16},
+              {cache_idx, "cache_idx", true, 4},
+              {q_segment_ids, "q_segment_ids", false, 4},
+              {kv_segment_ids, "kv_segment_ids", false, 4}};
+  for (const auto& x : ptrs) {
+    if (x.p == nullptr) {
+      if (x.required) return fail(RA_ERR_INVALID_ARG, "%s is NULL", x.name);
+      continue;
+    }
+    if (((uintptr_t)x.p % x.align) != 0)
+      return fail(RA_ERR_INVALID_ARG, "%s is not %d-byte aligned", x.name, (int)x.align);
+  }
+  const size_t need = decode_workspace_bytes(batch, new_tokens, cache_len, heads, head_dim, num_shards);
+  if (workspace_bytes < need)
+    return fail(RA_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", workspace_bytes, need);
+  if (need > 0 && (workspace == nullptr || !aligned16(workspace)))
+    return fail(RA_ERR_INVALID_ARG, "workspace is NULL or not 16-byte aligned");
+  Ctx c;
+  ra_status s = make_ctx(stream, &c);
+  if (s != RA_OK) return s;
+  DecodeArgs a;
+  a.B = batch;
+  a.T = new_tokens;
+  a.S = cache_len;
+  a.H = heads;
+  a.D = head_dim;
+  a.N = num_shards;
+  a.causal = causal_block_size;
+  a.bf16 = dtype == RA_BF16;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.cache_idx = cache_idx;
+  a.qseg = q_segment_ids;
+  a.kseg = kv_segment_ids;
+  a.out = out;
+  a.lse = lse;
+  a.workspace = workspace;
+  uint64_t n = 0;
+  cudaError_t e = launch_decode(a, c, &n);
+  g_launches += n;
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 RA_API ra_status ra_sync_check(void* stream) {
   Ctx c;
   ra_status s = make_ctx(stream, &c);

@@ -51,6 +51,32 @@ struct Ctx {
   cudaStream_t stream;
 };
 
+// Decoding T new tokens against a [B, S, H, D] KV cache.
+struct DecodeArgs {
+  int B, T, S, H, D, N, causal;
+  bool bf16;
+  const void* q;             // [B, T, H, D]
+  const void* k;             // [B, S, H, D]
+  const void* v;             // [B, S, H, D]
+  const int32_t* cache_idx;  // [B]
+  const int32_t* qseg;       // [B, T] or nullptr
+  const int32_t* kseg;       // [B, S] or nullptr
+  void* out;                 // [B, T, H, D]
+  float* lse;                // [B, H, T]
+  void* workspace;           // decode_workspace_bytes(...)
+};
+
+// How the cache is cut into work items (a function of the shape only, so that
+// the workspace size does not depend on the device).
+struct DecodeSplit {
+  int split_len;        // keys per work item
+  int items_per_shard;  // ceil((S / N) / split_len)
+  int P;                // partials per (b, h, token) = N * items_per_shard
+};
+DecodeSplit decode_split(int B, int T, int S, int H, int num_shards);
+size_t decode_workspace_bytes(int B, int T, int S, int H, int D, int num_shards);
+cudaError_t launch_decode(const DecodeArgs& a, const Ctx& c, uint64_t* launches);
+
 // Launchers.  Each returns the CUDA error of its launch(es) and adds the
 // number of kernels it launched to *launches.
 cudaError_t launch_fwd_f32(const FwdArgs& a, const Ctx& c, uint64_t* launches);

@@ -221,3 +221,93 @@ def sample_rows(seed: int, w: Workload, n: int) -> np.ndarray:
     is_ = g.integers(S, size=m)
     rows.extend(zip(bs.tolist(), hs.tolist(), is_.tolist()))
     return np.array(rows, dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# Decoding against a KV cache
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """T new tokens per batch row against a [B, S, H, D] key/value cache."""
+
+    name: str
+    batch: int
+    new_tokens: int
+    cache_len: int
+    heads: int
+    head_dim: int
+    dtype: str
+    causal_block_size: int
+    num_shards: int
+    scale: float = 1.0
+    segments: bool = False
+    fill: str = "full"  # "full": cache_idx = S - T for every row; "random": seeded draws
+    seed: int = 0
+    doc_len_range: tuple = field(default=(256, 8192))
+
+    def with_(self, **kw) -> "DecodeWorkload":
+        d = dict(self.__dict__)
+        d.update(kw)
+        return DecodeWorkload(**d)
+
+
+# Long-context decode with the 7B shape: the cache is the 131072-token K/V of
+# the 7B-shaped forward workload (same seed, same streams: identical values).
+DECODE_WORKLOADS = {
+    "7b": DecodeWorkload("7B-shaped decode B1 T1 S131072 H32 D128 bf16, 16 virtual shards, full cache",
+                         1, 1, 131072, 32, 128, "bf16", 1, 16, seed=1004),
+}
+
+
+@dataclass
+class DecodeInputs:
+    """Host arrays for one decode problem.  bf16 tensors are uint16 bit patterns."""
+
+    w: DecodeWorkload
+    q: np.ndarray            # [B, T, H, D]
+    k_cache: np.ndarray      # [B, S, H, D]
+    v_cache: np.ndarray      # [B, S, H, D]
+    cache_idx: np.ndarray    # [B] int32
+    q_segment_ids: np.ndarray | None   # [B, T] int32
+    kv_segment_ids: np.ndarray | None  # [B, S] int32
+
+    def as_f64(self, name: str) -> np.ndarray:
+        x = getattr(self, name)
+        if self.w.dtype == "bf16":
+            return bf16_bits_to_f32(x).astype(np.float64)
+        return x.astype(np.float64)
+
+
+def decode_cache_idx(seed: int, batch: int, new_tokens: int, cache_len: int, fill: str) -> np.ndarray:
+    """[B] int32 cache indices: "full" -> S - T; "random" -> U[0, S - T] per row
+    with row 0 forced to S - T and row 1 (if any) to 0."""
+    top = max(0, cache_len - new_tokens)
+    if fill == "full":
+        return np.full(batch, top, dtype=np.int32)
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 31])))
+    idx = g.integers(0, top, size=batch, endpoint=True).astype(np.int32)
+    idx[0] = top
+    if batch > 1:
+        idx[1] = 0
+    return idx
+
+
+def make_decode_inputs(w: DecodeWorkload, cache_idx=None) -> DecodeInputs:
+    cshape = (w.batch, w.cache_len, w.heads, w.head_dim)
+    k = tensor(w.seed, 1, cshape, w.scale, w.dtype)
+    v = tensor(w.seed, 2, cshape, w.scale, w.dtype)
+    q = tensor(w.seed, 4, (w.batch, w.new_tokens, w.heads, w.head_dim), w.scale, w.dtype)
+    if cache_idx is None:
+        cache_idx = decode_cache_idx(w.seed, w.batch, w.new_tokens, w.cache_len, w.fill)
+    cache_idx = np.asarray(cache_idx, dtype=np.int32)
+    qseg = kseg = None
+    if w.segments:
+        lo, hi = w.doc_len_range
+        kseg = packed_segment_ids(w.seed, w.batch, w.cache_len, lo, hi)
+        qseg = np.zeros((w.batch, w.new_tokens), dtype=np.int32)
+        for b in range(w.batch):  # a new token belongs to the document of its cache position
+            for t in range(w.new_tokens):
+                j = int(cache_idx[b]) + t
+                qseg[b, t] = kseg[b, min(max(j, 0), w.cache_len - 1)] if w.cache_len > 0 else 0
+    return DecodeInputs(w, q, k, v, cache_idx, qseg, kseg)

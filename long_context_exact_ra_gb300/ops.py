@@ -20,7 +20,8 @@ RA_F32, RA_BF16 = 0, 1
 _STATUS = {1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "device wait timed out"}
 
 EXPORTS = ("ra_fwd", "ra_bwd", "ra_bwd_workspace_size", "ra_sync_check", "ra_last_error",
-           "ra_kernel_launches", "ra_selftest_timeout", "ra_bwd_noalloc", "ra_bwd_noalloc_max_scratch")
+           "ra_kernel_launches", "ra_selftest_timeout", "ra_bwd_noalloc", "ra_bwd_noalloc_max_scratch",
+           "ra_decode", "ra_decode_workspace_size")
 
 
 class RAError(RuntimeError):
@@ -61,6 +62,10 @@ def lib() -> ctypes.CDLL:
                                  vp, vp, vp, vp]
     L.ra_bwd_noalloc_max_scratch.restype = sz
     L.ra_bwd_noalloc_max_scratch.argtypes = []
+    L.ra_decode_workspace_size.restype = sz
+    L.ra_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    L.ra_decode.restype = i32
+    L.ra_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, sz, vp]
     _lib = L
     return L
 
@@ -177,6 +182,49 @@ def bwd_noalloc(q, k, v, out, lse, dout, segment_ids=None, causal_block_size=0, 
                                 int(causal_block_size), int(num_shards), int(qc), int(kc), B, S, H, D,
                                 _dtype_code(q), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
     return dq, dk, dv
+
+
+def decode_workspace_size(B, T, S, H, D, num_shards, dtype) -> int:
+    code = RA_BF16 if dtype == torch.bfloat16 else RA_F32
+    return int(lib().ra_decode_workspace_size(B, T, S, H, D, num_shards, code))
+
+
+def decode(q, k_cache, v_cache, cache_idx, q_segment_ids=None, kv_segment_ids=None,
+           causal_block_size=1, num_shards=1, out=None, lse=None, workspace=None, stream=None):
+    """ra_decode: T new tokens q [B,T,H,D] against the cache [B,S,H,D] at cache_idx [B] (int32).
+
+    Returns (out [B,T,H,D] like q, lse [B,H,T] float32)."""
+    _check_tensor("q", q)
+    B, T, H, D = q.shape
+    _check_tensor("k_cache", k_cache)
+    _check_tensor("v_cache", v_cache, k_cache)
+    if k_cache.dtype != q.dtype or k_cache.shape[0] != B or k_cache.shape[2] != H or k_cache.shape[3] != D:
+        raise ValueError("k_cache must be [B, S, H, D] with q's dtype, batch, heads and head_dim")
+    S = k_cache.shape[1]
+    _check_tensor("cache_idx", cache_idx, dtype=torch.int32)
+    if tuple(cache_idx.shape) != (B,):
+        raise ValueError("cache_idx must be [batch]")
+    if (q_segment_ids is None) != (kv_segment_ids is None):
+        raise ValueError("q_segment_ids and kv_segment_ids must be given together")
+    if q_segment_ids is not None:
+        _check_tensor("q_segment_ids", q_segment_ids, dtype=torch.int32)
+        _check_tensor("kv_segment_ids", kv_segment_ids, dtype=torch.int32)
+        if tuple(q_segment_ids.shape) != (B, T) or tuple(kv_segment_ids.shape) != (B, S):
+            raise ValueError("segment ids must be [batch, new_tokens] and [batch, cache_len]")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    _check_tensor("out", out, q)
+    _check_tensor("lse", lse, dtype=torch.float32)
+    need = decode_workspace_size(B, T, S, H, D, num_shards, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().ra_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_idx), _ptr(q_segment_ids),
+                           _ptr(kv_segment_ids), int(causal_block_size), int(num_shards), B, T, S, H, D,
+                           _dtype_code(q), _ptr(out), _ptr(lse), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse
 
 
 def sync_check(stream=None):

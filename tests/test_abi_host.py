@@ -82,3 +82,35 @@ def test_bwd_validation_and_workspace(L):
 def test_selftest_limit_is_validated(L):
     assert L.ra_selftest_timeout(0, None) == ops.RA_ERR_INVALID_ARG
     assert L.ra_selftest_timeout(2_000_000_000, None) == ops.RA_ERR_INVALID_ARG
+
+
+def _dec(L, q=16, k=16, v=16, idx=16, qseg=None, kseg=None, c=1, N=1, B=1, T=1, S=128, H=1, D=128, dt=1,
+         out=16, lse=16, ws=16, wsb=1 << 30):
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return L.ra_decode(P(q), P(k), P(v), P(idx), P(qseg), P(kseg), c, N, B, T, S, H, D, dt, P(out), P(lse),
+                       P(ws), ctypes.c_size_t(wsb), None)
+
+
+def test_decode_validation_and_workspace(L):
+    assert _dec(L, q=None) == ops.RA_ERR_INVALID_ARG and b"q is NULL" in L.ra_last_error()
+    assert _dec(L, idx=None) == ops.RA_ERR_INVALID_ARG and b"cache_idx" in L.ra_last_error()
+    assert _dec(L, idx=18) == ops.RA_ERR_INVALID_ARG  # int32 array not 4-byte aligned
+    assert _dec(L, k=24) == ops.RA_ERR_INVALID_ARG and b"16-byte" in L.ra_last_error()
+    assert _dec(L, qseg=16) == ops.RA_ERR_INVALID_ARG  # segment ids must come in pairs
+    assert _dec(L, S=130, N=4) == ops.RA_ERR_INVALID_ARG
+    assert _dec(L, c=-1) == ops.RA_ERR_INVALID_ARG
+    assert _dec(L, N=0) == ops.RA_ERR_INVALID_ARG
+    assert _dec(L, B=0) == ops.RA_ERR_INVALID_ARG
+    assert _dec(L, B=70000) == ops.RA_ERR_INVALID_ARG
+    assert _dec(L, dt=5) == ops.RA_ERR_INVALID_ARG
+    assert _dec(L, D=96) == ops.RA_ERR_UNSUPPORTED
+    assert _dec(L, T=65) == ops.RA_ERR_UNSUPPORTED
+    assert _dec(L, wsb=8) == ops.RA_ERR_INVALID_ARG and b"workspace" in L.ra_last_error()
+    # no new token: nothing to do, no GPU touched
+    assert _dec(L, T=0) == ops.RA_OK and L.ra_last_error() == b""
+    # the workspace is a function of the shape: partial (m, l, o) per (b, h, token, work item)
+    ws1 = L.ra_decode_workspace_size(1, 1, 131072, 32, 128, 16, 1)
+    ws2 = L.ra_decode_workspace_size(1, 2, 131072, 32, 128, 16, 1)
+    assert ws1 > 0 and ws2 >= 2 * ws1 - 512 and ws1 % 256 == 0
+    assert L.ra_decode_workspace_size(1, 1, 0, 1, 64, 1, 1) == 0
+    assert L.ra_decode_workspace_size(0, 1, 128, 1, 64, 1, 1) == 0
