@@ -5,7 +5,9 @@ A step is one pass of the whole hot path on the default workload: the causal
 bf16 forward AND backward at batch 1, seq 65536, 32 heads, head_dim 128, 8
 virtual ring shards (ra_fwd then ra_bwd).  The same run also times the
 long-context forward (seq 131072, 32 heads, 16 shards) and reports it under
-"fwd_s131072".  Inputs are seeded synthetic N(0,1) bf16 tensors, resident in
+"fwd_s131072", and decoding one new token against that 131072-token K/V as
+a full KV cache (ra_decode, HBM-bound) under "decode_s131072".  Inputs are
+seeded synthetic N(0,1) bf16 tensors, resident in
 HBM before the timed region; every input set is larger than the 129 MB L2, so
 no flush is needed between steps.
 
@@ -36,7 +38,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from long_context_exact_ra_gb300 import flops as F  # noqa: E402
-from long_context_exact_ra_gb300.inputs import WORKLOADS, make_inputs, sample_rows  # noqa: E402
+from long_context_exact_ra_gb300.inputs import (DECODE_WORKLOADS, WORKLOADS, decode_cache_idx,  # noqa: E402
+                                                make_inputs, sample_rows, tensor)
 
 METRIC = "attention TFLOP/s (causal bf16 fwd/bwd, 1xGB300) and % of dense BF16 tensor peak"
 UNIT = "TFLOP/s"
@@ -158,8 +161,9 @@ def to_pinned(x, torch):
     return t.pin_memory()
 
 
-def time_fwd(ops, torch, w, steps, warmup, dev):
-    """Forward-only timing of workload w (device-resident inputs)."""
+def time_fwd(ops, torch, w, steps, warmup, dev, keep_kv=False):
+    """Forward-only timing of workload w (device-resident inputs).  With keep_kv
+    the device K and V are returned too (the decode leg reads them as its cache)."""
     x = make_inputs(w, with_dout=False)
     q, k, v = (to_dev(getattr(x, n), torch, dev) for n in ("q", "k", "v"))
     del x
@@ -180,7 +184,42 @@ def time_fwd(ops, torch, w, steps, warmup, dev):
     ops.sync_check()
     ms = [a.elapsed_time(b) for a, b in evs]
     fl = F.fwd_flops_nominal(w.batch, w.seq, w.heads, w.head_dim, w.causal_block_size > 0)
+    if keep_kv:
+        return fl, ms, (k, v)
     return fl, ms
+
+
+def time_decode(ops, torch, wd, kv, iters, warmup, dev):
+    """ra_decode of the decode workload wd against the device cache kv = (k, v)
+    ([B, S, H, D] bf16, S = wd.cache_len); the new tokens' q is drawn from the
+    decode inputs' own stream.  Returns (ms per call, algorithmic bytes per call)."""
+    k, v = kv
+    B, T, S, H, D = wd.batch, wd.new_tokens, wd.cache_len, wd.heads, wd.head_dim
+    assert tuple(k.shape) == (B, S, H, D)
+    q = to_dev(tensor(wd.seed, 4, (B, T, H, D), wd.scale, wd.dtype), torch, dev)
+    idx_h = decode_cache_idx(wd.seed, B, T, S, wd.fill)
+    idx = torch.from_numpy(idx_h).to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    work = torch.empty(max(16, ops.decode_workspace_size(B, T, S, H, D, wd.num_shards, torch.bfloat16)),
+                       dtype=torch.uint8, device=dev)
+    call = lambda: ops.decode(q, k, v, idx, None, None, wd.causal_block_size, wd.num_shards,  # noqa: E731
+                              out=out, lse=lse, workspace=work)
+    for _ in range(warmup):
+        call()
+    ops.sync_check()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(iters):
+        call()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ops.sync_check()
+    filled = np.clip(idx_h.astype(np.int64) + T, 0, S)
+    byts = int(filled.sum()) * H * D * 2 * 2  # K and V rows of the filled cache, bf16
+    return e0.elapsed_time(e1) / iters, byts
 
 
 def run_e2e(args, torch, d, host, names, step, out, lse, backward, grads, st, ws, dev):
@@ -338,12 +377,25 @@ def gpu_arm(args, peaks, peaks_src):
             del dq, dk, dv, work
         torch.cuda.empty_cache()
         w4 = WORKLOADS[4]
-        fl4, ms4 = time_fwd(ops, torch, w4, max(3, args.steps), args.warmup, dev)
+        fl4, ms4, kv4 = time_fwd(ops, torch, w4, max(3, args.steps), args.warmup, dev, keep_kv=True)
         tf4 = fl4 / (statistics.mean(ms4) * 1e-3) / 1e12
         extra["fwd_s131072"] = {"workload": w4.name, "tflops": round(tf4, 1), "frac": round(tf4 / peak, 4),
                                 "frac_sustained": round(tf4 / peak_s, 4), "ms": round(statistics.mean(ms4), 3),
                                 "flops": fl4,
                                 "traffic": profile_traffic("fwd128_cfg4", fwd_sha)}
+        # decode: one new token against that 131072-token K/V as a full cache (HBM-bound)
+        wd = DECODE_WORKLOADS["7b"]
+        dms, dbytes = time_decode(ops, torch, wd, kv4, max(20, 10 * args.steps), max(3, args.warmup), dev)
+        del kv4
+        gbs = dbytes / (dms * 1e-3) / 1e9
+        hbm = peaks["hbm_gbs"]
+        dec_sha = source_sha("decode_sm103.cu")
+        extra["decode_s131072"] = {
+            "workload": wd.name, "ms": round(dms, 4), "tokens_per_s": round(wd.batch * wd.new_tokens / (dms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "kernel": "ra_decode (partial + combine)", "achieved": round(gbs, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_source": peaks_src,
+                         "algorithmic_bytes": dbytes,
+                         "traffic": profile_traffic("decode128_7b", dec_sha)}}
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
@@ -443,7 +495,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, choices=[2, 3, 4, 5], default=5)
-    ap.add_argument("--no-secondary", action="store_true", help="skip the seq-131072 forward line")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the seq-131072 forward and decode lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--seq", type=int, default=0, help="run a smaller seq of the workload (profiling)")
