@@ -251,7 +251,7 @@ def run_e2e(args, torch, d, host, names, step, out, lse, backward, grads, st, ws
     e1.record(st)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
-    h2d = sum(host[n].numel() * 2 for n in names)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     d2h = sum(t.numel() * 2 for t in hout.values()) + hlse.numel() * 4
     return e2e_ms, h2d, d2h
 
@@ -282,12 +282,17 @@ def gpu_arm(args, peaks, peaks_src):
     x = make_inputs(w, with_dout=backward)
     names = ("q", "k", "v") + (("dout",) if backward else ())
     host = {n: to_pinned(getattr(x, n), torch) for n in names}
+    seg_h = x.segment_ids
     del x
     d = {n: host[n].to(dev) for n in names}
+    if seg_h is not None:  # packed documents: the segment ids are an input like q, k, v
+        host["seg"] = torch.from_numpy(np.ascontiguousarray(seg_h)).pin_memory()
+        d["seg"] = host["seg"].to(dev)
+        names = names + ("seg",)
     B, S, H, D = w.shape
     out = torch.empty_like(d["q"])
     lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
-    cargs = (None, w.causal_block_size, w.num_shards, w.query_chunk_size, w.key_chunk_size)
+    cargs = (d.get("seg"), w.causal_block_size, w.num_shards, w.query_chunk_size, w.key_chunk_size)
     if backward:
         dq, dk, dv = (torch.empty_like(d["q"]) for _ in range(3))
         wsz = ops.bwd_workspace_size(B, S, H, D, torch.bfloat16)
@@ -350,12 +355,18 @@ def gpu_arm(args, peaks, peaks_src):
     peak = peaks["bf16_tflops"]
     peak_s = peaks.get("bf16_tflops_sustained", peak)
     fwd_tf = fl_f / (fwd_ms * 1e-3) / 1e12
+    # visible-pair work (differs from the nominal formula when segments mask most of the square)
+    fl_vis = F.fwd_flops_visible(B, S, H, D, w.causal_block_size, seg_h) if seg_h is not None else None
     fwd_sha = source_sha("attn_fwd_sm103.cu", "sm103.cuh")
     roof_fwd = {"bound": "tensor", "kernel": f"fwd_bf16_kernel<{D}>", "achieved": round(fwd_tf, 1),
                 "peak": peak, "unit": UNIT, "frac": round(fwd_tf / peak, 4),
                 "frac_sustained": round(fwd_tf / peak_s, 4), "peak_source": peaks_src,
                 "traffic": profile_traffic(f"fwd{D}_cfg{args.workload}", fwd_sha),
                 "ms_per_launch": round(fwd_ms, 3), "flops_per_launch": fl_f}
+    if fl_vis is not None:
+        vis_tf = fl_vis / (fwd_ms * 1e-3) / 1e12
+        roof_fwd.update({"visible_flops_per_launch": fl_vis, "achieved_visible": round(vis_tf, 1),
+                         "frac_visible": round(vis_tf / peak, 4)})
     roofline = roof_fwd
     extra = {}
     if backward:
@@ -442,7 +453,15 @@ def oracle_rows_rate(w, budget_s, x=None, start_rows=32):
         t = time.perf_counter()
         oracle.ref_fwd_rows(q, k, v, rows, x.segment_ids, c)
         total_t += time.perf_counter() - t
-        if c > 0:
+        if x.segment_ids is not None:  # count the keys each sampled row actually sees
+            kpos = np.arange(w.seq)
+            seg = x.segment_ids[bh[0]]
+            for i in rows[:, 2]:
+                ok = seg == seg[i]
+                if c > 0:
+                    ok &= (kpos // c) <= (i // c)
+                total_f += 4.0 * w.head_dim * np.count_nonzero(ok)
+        elif c > 0:
             vis = ((rows[:, 2] // c) + 1) * c
             total_f += 4.0 * w.head_dim * np.minimum(vis, w.seq).sum()
         else:

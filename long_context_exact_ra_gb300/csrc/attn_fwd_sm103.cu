@@ -259,11 +259,20 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
             bool needed = !(c > 0 && floordiv_pos(qlast, c) < floordiv_pos(ka, c));
             int mn = INT_MAX, mx = INT_MIN;
             if (needed) {
-              const int* sp = pb.seg + (size_t)b * pb.S;
-              for (int x = ka; x < kb; ++x) {
-                const int sv = __ldg(sp + x);
-                mn = min(mn, sv);
-                mx = max(mx, sv);
+              const int* sp = pb.seg + (size_t)b * pb.S + ka;
+              if (kb - ka == kBN && ((reinterpret_cast<uintptr_t>(sp) & 15u) == 0)) {
+#pragma unroll 8
+                for (int x4 = 0; x4 < kBN / 4; ++x4) {
+                  const int4 sv = __ldg(reinterpret_cast<const int4*>(sp) + x4);
+                  mn = min(mn, min(min(sv.x, sv.y), min(sv.z, sv.w)));
+                  mx = max(mx, max(max(sv.x, sv.y), max(sv.z, sv.w)));
+                }
+              } else {
+                for (int x = 0; x < kb - ka; ++x) {
+                  const int sv = __ldg(sp + x);
+                  mn = min(mn, sv);
+                  mx = max(mx, sv);
+                }
               }
             }
             kmn = mn;
@@ -526,17 +535,37 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
 #pragma unroll
         for (int cq = 0; cq < 4; ++cq) tmem_ld_wait(sr + cq * 32);
         if (r.flags & (w == 0 ? kMask0 : kMask1)) {
-          const int cb = pb.causal;
-          const int qblk = cb > 0 ? qrow / cb : 0;
-          const int qseg = pb.seg ? __ldg(pb.seg + (size_t)r.b * pb.S + min(qrow, pb.S - 1)) : 0;
-          const int* kseg = pb.seg ? pb.seg + (size_t)r.b * pb.S : nullptr;
+          // keys x < nvis of the tile pass the range and causal rules: the causal
+          // block of key kstart + x must not exceed the row's block
+          long long lim = r.kvalid;
+          if (pb.causal > 0) lim = min(lim, ((long long)qrow / pb.causal + 1) * pb.causal - r.kstart);
+          const int nvis = (int)max(lim, 0LL);
+          if (pb.seg) {
+            const int* ks = pb.seg + (size_t)r.b * pb.S + r.kstart;
+            const int qseg = __ldg(pb.seg + (size_t)r.b * pb.S + min(qrow, pb.S - 1));
+            if (r.kvalid == 128 && ((reinterpret_cast<uintptr_t>(ks) & 15u) == 0)) {
+              // the tile's 128 key ids in 16-byte loads (the same addresses for every row: L1 broadcast)
 #pragma unroll
-          for (int x = 0; x < 128; ++x) {
-            const int key = r.kstart + x;
-            bool vis = x < r.kvalid;
-            if (cb > 0) vis = vis && (qblk >= key / cb);
-            if (kseg) vis = vis && (__ldg(kseg + min(key, pb.S - 1)) == qseg);
-            if (!vis) sr[x] = __float_as_uint(-INFINITY);
+              for (int x4 = 0; x4 < 32; ++x4) {
+                const int4 sv = __ldg(reinterpret_cast<const int4*>(ks) + x4);
+                const int e[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int x = 4 * x4 + i;
+                  if (!(x < nvis && e[i] == qseg)) sr[x] = __float_as_uint(-INFINITY);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int x = 0; x < 128; ++x) {
+                const bool vis = x < nvis && __ldg(ks + min(x, r.kvalid - 1)) == qseg;
+                if (!vis) sr[x] = __float_as_uint(-INFINITY);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int x = 0; x < 128; ++x)
+              if (!(x < nvis)) sr[x] = __float_as_uint(-INFINITY);
           }
         }
         // row max: eight independent chains of three-input max
