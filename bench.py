@@ -434,6 +434,34 @@ def gpu_arm(args, peaks, peaks_src):
         print(json.dumps(result), flush=True)
 
 
+def decode_arm(args, peaks, peaks_src):
+    """--decode-only: the decode leg alone (profiling; cache_len = --seq, default 131072)."""
+    import torch
+
+    from long_context_exact_ra_gb300 import ops
+    from long_context_exact_ra_gb300.inputs import make_decode_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ops.lib()
+    wd = DECODE_WORKLOADS["7b"]
+    if args.seq:
+        wd = wd.with_(name=f"{wd.name} at cache_len {args.seq}", cache_len=args.seq)
+    x = make_decode_inputs(wd)
+    kv = (to_dev(x.k_cache, torch, dev), to_dev(x.v_cache, torch, dev))
+    del x
+    dms, dbytes = time_decode(ops, torch, wd, kv, max(1, args.steps), max(1, args.warmup), dev)
+    gbs = dbytes / (dms * 1e-3) / 1e9
+    hbm = peaks["hbm_gbs"]
+    print(json.dumps({"metric": "decode KV-cache read GB/s (ra_decode)", "value": round(gbs, 1), "unit": "GB/s",
+                      "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dms, 4),
+                      "higher_is_better": True, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
+                      "config": {"workload": wd.name, "note": "decode leg alone, for profiling"},
+                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                                   "frac": round(gbs / hbm, 4), "peak_source": peaks_src,
+                                   "algorithmic_bytes": dbytes}}), flush=True)
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_rows_rate(w, budget_s, x=None, start_rows=32):
     """Time the float64 oracle on sampled query rows of workload w; return
@@ -514,6 +542,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, choices=[2, 3, 4, 5], default=5)
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the decode leg (cache_len = --seq, default 131072); for profiling")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the seq-131072 forward and decode lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -526,6 +556,8 @@ def main():
     peaks, src = load_peaks()
     if args.impl == "reference":
         reference_arm(args)
+    elif args.decode_only:
+        decode_arm(args, peaks, src)
     else:
         gpu_arm(args, peaks, src)
 
