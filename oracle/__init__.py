@@ -20,3 +20,4 @@ from .decode import (  # noqa: F401
     ref_decode_rows,
     ref_ring_decode,
 )
+from .ffn import ffn_rows, ref_blockwise_ffn  # noqa: F401
