@@ -6,7 +6,8 @@ bf16 forward AND backward at batch 1, seq 65536, 32 heads, head_dim 128, 8
 virtual ring shards (ra_fwd then ra_bwd).  The same run also times the
 long-context forward (seq 131072, 32 heads, 16 shards) and reports it under
 "fwd_s131072", and decoding one new token against that 131072-token K/V as
-a full KV cache (ra_decode, HBM-bound) under "decode_s131072".  Inputs are
+a full KV cache (ra_decode, HBM-bound) under "decode_s131072", and the blockwise
+feed-forward at the 7B shape (ra_blockwise_ffn) under "ffn_7b".  Inputs are
 seeded synthetic N(0,1) bf16 tensors, resident in
 HBM before the timed region; every input set is larger than the 129 MB L2, so
 no flush is needed between steps.
@@ -38,8 +39,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from long_context_exact_ra_gb300 import flops as F  # noqa: E402
-from long_context_exact_ra_gb300.inputs import (DECODE_WORKLOADS, WORKLOADS, decode_cache_idx,  # noqa: E402
-                                                make_inputs, sample_rows, tensor)
+from long_context_exact_ra_gb300.inputs import (DECODE_WORKLOADS, FFN_WORKLOADS, WORKLOADS,  # noqa: E402
+                                                decode_cache_idx, make_ffn_inputs, make_inputs, sample_rows,
+                                                tensor)
 
 METRIC = "attention TFLOP/s (causal bf16 fwd/bwd, 1xGB300) and % of dense BF16 tensor peak"
 UNIT = "TFLOP/s"
@@ -407,6 +409,17 @@ def gpu_arm(args, peaks, peaks_src):
                          "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_source": peaks_src,
                          "algorithmic_bytes": dbytes,
                          "traffic": profile_traffic("decode128_7b", dec_sha)}}
+        # blockwise feed-forward at the 7B shape (the other half of a blockwise transformer layer)
+        wf = FFN_WORKLOADS["7b"]
+        fms, ffl = time_ffn(ops, torch, wf, max(5, args.steps), max(3, args.warmup), dev)
+        ftf = ffl / (fms * 1e-3) / 1e12
+        extra["ffn_7b"] = {
+            "workload": wf.name, "ms": round(fms, 3),
+            "roofline": {"bound": "tensor", "kernel": "gemm_bias_act_kernel (2 launches per chunk)",
+                         "achieved": round(ftf, 1), "peak": peak, "unit": UNIT, "frac": round(ftf / peak, 4),
+                         "frac_sustained": round(ftf / peak_s, 4), "peak_source": peaks_src,
+                         "flops_per_launch": ffl,
+                         "traffic": profile_traffic("ffn_7b", source_sha("ffn_sm103.cu", "sm103.cuh"))}}
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
@@ -460,6 +473,32 @@ def decode_arm(args, peaks, peaks_src):
                       "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                                    "frac": round(gbs / hbm, 4), "peak_source": peaks_src,
                                    "algorithmic_bytes": dbytes}}), flush=True)
+
+
+def time_ffn(ops, torch, wf, iters, warmup, dev):
+    """ra_blockwise_ffn on workload wf (device-resident inputs); returns (ms per call, FLOPs per call)."""
+    xi = make_ffn_inputs(wf)
+    x, w1, w2 = (to_dev(a, torch, dev) for a in (xi.x, xi.w1, xi.w2))
+    b1 = torch.from_numpy(xi.b1).to(dev) if xi.b1 is not None else None
+    b2 = torch.from_numpy(xi.b2).to(dev) if xi.b2 is not None else None
+    del xi
+    out = torch.empty_like(x)
+    work = torch.empty(ops.ffn_workspace_size(wf.batch, wf.seq, wf.ffn_dim, wf.chunk_size), dtype=torch.uint8,
+                       device=dev)
+    for _ in range(warmup):
+        ops.blockwise_ffn(x, w1, b1, w2, b2, wf.chunk_size, out=out, workspace=work)
+    ops.sync_check()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(iters):
+        ops.blockwise_ffn(x, w1, b1, w2, b2, wf.chunk_size, out=out, workspace=work)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ops.sync_check()
+    flops = 2.0 * 2 * wf.batch * wf.seq * wf.model_dim * wf.ffn_dim  # two products
+    return e0.elapsed_time(e1) / iters, flops
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -545,7 +584,7 @@ def main():
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode leg (cache_len = --seq, default 131072); for profiling")
     ap.add_argument("--no-secondary", action="store_true",
-                    help="skip the seq-131072 forward and decode lines")
+                    help="skip the seq-131072 forward, decode and feed-forward lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--seq", type=int, default=0, help="run a smaller seq of the workload (profiling)")

@@ -153,6 +153,36 @@ ra_status ra_decode(const void* q, const void* k_cache, const void* v_cache,
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Blockwise feed-forward network (the other half of a blockwise transformer
+ * layer): out = FFN(x) = max(0, x W1 + b1) W2 + b2 for every row (paper review
+ * page), computed on chunks of `chunk_size` rows of the flattened
+ * (batch * seq) axis one after another, so that only one chunk's hidden
+ * activation exists at a time ("Blockwise Feedforward网络详解RingAttention如何
+ * 实现内存高效的前向传播", §核心技术原理, §分块重组机制).  The result does not
+ * depend on chunk_size.
+ * Layouts (row-major, contiguous, device memory, bf16 unless noted):
+ *   x, out     : [batch, seq, model_dim]
+ *   w1         : [ffn_dim, model_dim]  (W1 transposed, as a linear layer stores it)
+ *   w2         : [model_dim, ffn_dim]  (W2 transposed)
+ *   b1, b2     : [ffn_dim], [model_dim] float32, or NULL for no bias
+ *   workspace  : ra_ffn_workspace_size(...) bytes: one chunk's hidden activation,
+ *                [min(batch*seq, chunk_size), ffn_dim] bf16 (contents on entry do not matter)
+ * Numerics: products in bf16 on the tensor cores with fp32 accumulation; the
+ * bias and ReLU are applied in fp32, and the hidden activation is rounded to
+ * bf16 once (it is stored in that type between the two products).
+ * Supported: dtype RA_BF16.  Requirements (else RA_ERR_INVALID_ARG): batch,
+ * model_dim, ffn_dim, chunk_size >= 1, seq >= 0 (0 returns RA_OK at once),
+ * model_dim and ffn_dim multiples of 8, batch*seq < 2^31, non-NULL tensor
+ * pointers (b1, b2 may be NULL), every pointer 16-byte aligned.  Two kernel
+ * launches per chunk on `stream`, asynchronous.
+ */
+size_t ra_ffn_workspace_size(int batch, int seq, int ffn_dim, int chunk_size);
+
+ra_status ra_blockwise_ffn(const void* x, const void* w1, const float* b1, const void* w2, const float* b2,
+                           int batch, int seq, int model_dim, int ffn_dim, int chunk_size, ra_dtype dtype,
+                           void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronize `stream`, then read and clear the device status word that the
  * kernels set when a bounded wait runs out.  Returns RA_ERR_TIMEOUT (message
  * names the wait site) if any kernel gave up since the last check,

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libra.so")
 
-SOURCES = ["ra_api.cu", "attn_f32.cu", "attn_fwd_sm103.cu", "attn_bwd_sm103.cu", "selftest.cu", "ra_noalloc.cu", "decode_sm103.cu"]
+SOURCES = ["ra_api.cu", "attn_f32.cu", "attn_fwd_sm103.cu", "attn_bwd_sm103.cu", "selftest.cu", "ra_noalloc.cu", "decode_sm103.cu", "ffn_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -486,37 +486,37 @@ __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(DecPara
 }
 
 template <typename E, int D, int TM>
-cudaError_t launch_partial(const DecParams& p, dim3 grid, cudaStream_t st) {
+cudaError_t launch_partial(const DecParams& p, dim3 grid, const Ctx& c) {
   constexpr int smem = dec_smem_bytes<E, D, TM>();
-  static bool attr_set = false;  // the attribute is per kernel and idempotent
-  if (!attr_set) {
+  static bool attr_set[256];  // the attribute is per kernel and device, and idempotent
+  if (!attr_set[c.device]) {
     cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<E, D, TM>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[c.device] = true;
   }
-  decode_partial_kernel<E, D, TM><<<grid, DecShape<E, D>::WARPS * 32, smem, st>>>(p);
+  decode_partial_kernel<E, D, TM><<<grid, DecShape<E, D>::WARPS * 32, smem, c.stream>>>(p);
   return cudaGetLastError();
 }
 
 template <typename E, int D>
-cudaError_t launch_typed(const DecParams& p, cudaStream_t st, uint64_t* launches) {
+cudaError_t launch_typed(const DecParams& p, const Ctx& c, uint64_t* launches) {
   const dim3 g1((unsigned)((long long)p.N * p.items_per_shard * p.H * p.tgroups), p.B);
   if (g1.x > 0) {
     cudaError_t e;
     if (p.T == 1) {
-      e = launch_partial<E, D, 1>(p, g1, st);
+      e = launch_partial<E, D, 1>(p, g1, c);
     } else if (p.T == 2) {
-      e = launch_partial<E, D, 2>(p, g1, st);
+      e = launch_partial<E, D, 2>(p, g1, c);
     } else if (p.T <= 4) {
-      e = launch_partial<E, D, 4>(p, g1, st);
+      e = launch_partial<E, D, 4>(p, g1, c);
     } else {
-      e = launch_partial<E, D, kTokGroup>(p, g1, st);
+      e = launch_partial<E, D, kTokGroup>(p, g1, c);
     }
     ++*launches;
     if (e != cudaSuccess) return e;
   }
-  decode_combine_kernel<E, D><<<dim3(p.T, p.H, p.B), kCombWarps * 32, 0, st>>>(p);
+  decode_combine_kernel<E, D><<<dim3(p.T, p.H, p.B), kCombWarps * 32, 0, c.stream>>>(p);
   ++*launches;
   return cudaGetLastError();
 }
@@ -578,10 +578,10 @@ cudaError_t launch_decode(const DecodeArgs& a, const Ctx& c, uint64_t* launches)
   p.lse = a.lse;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)a.D);
   if (a.bf16) {
-    return a.D == 128 ? launch_typed<__nv_bfloat16, 128>(p, c.stream, launches)
-                      : launch_typed<__nv_bfloat16, 64>(p, c.stream, launches);
+    return a.D == 128 ? launch_typed<__nv_bfloat16, 128>(p, c, launches)
+                      : launch_typed<__nv_bfloat16, 64>(p, c, launches);
   }
-  return a.D == 128 ? launch_typed<float, 128>(p, c.stream, launches) : launch_typed<float, 64>(p, c.stream, launches);
+  return a.D == 128 ? launch_typed<float, 128>(p, c, launches) : launch_typed<float, 64>(p, c, launches);
 }
 
 }  // namespace ra

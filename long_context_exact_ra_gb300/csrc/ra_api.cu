@@ -295,6 +295,65 @@ RA_API ra_status ra_decode(const void* q, const void* k_cache, const void* v_cac
   return ok();
 }
 
+RA_API size_t ra_ffn_workspace_size(int batch, int seq, int ffn_dim, int chunk_size) {
+  if (batch < 1 || seq < 0 || ffn_dim < 1 || chunk_size < 1) return 0;
+  return ffn_workspace_bytes((long long)batch * seq, chunk_size, ffn_dim);
+}
+
+RA_API ra_status ra_blockwise_ffn(const void* x, const void* w1, const float* b1, const void* w2, const float* b2,
+                                  int batch, int seq, int model_dim, int ffn_dim, int chunk_size, ra_dtype dtype,
+                                  void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (batch < 1 || seq < 0 || model_dim < 1 || ffn_dim < 1 || chunk_size < 1)
+    return fail(RA_ERR_INVALID_ARG, "bad shape batch=%d seq=%d model_dim=%d ffn_dim=%d chunk_size=%d", batch, seq,
+                model_dim, ffn_dim, chunk_size);
+  if (model_dim % 8 != 0 || ffn_dim % 8 != 0)
+    return fail(RA_ERR_INVALID_ARG, "model_dim (%d) and ffn_dim (%d) must be multiples of 8", model_dim, ffn_dim);
+  if ((long long)batch * seq >= (1LL << 31))
+    return fail(RA_ERR_INVALID_ARG, "batch * seq must be < 2^31");
+  if (dtype != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "the blockwise feed-forward supports bf16 only");
+  if (seq == 0) return ok();
+  struct {
+    const void* p;
+    const char* name;
+    bool required;
+  } ptrs[] = {{x, "x", true}, {w1, "w1", true}, {w2, "w2", true}, {out, "out", true},
+              {workspace, "workspace", true}, {b1, "b1", false}, {b2, "b2", false}};
+  for (const auto& q : ptrs) {
+    if (q.p == nullptr) {
+      if (q.required) return fail(RA_ERR_INVALID_ARG, "%s is NULL", q.name);
+      continue;
+    }
+    if (!aligned16(q.p)) return fail(RA_ERR_INVALID_ARG, "%s is not 16-byte aligned", q.name);
+  }
+  const size_t need = ffn_workspace_bytes((long long)batch * seq, chunk_size, ffn_dim);
+  if (workspace_bytes < need)
+    return fail(RA_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", workspace_bytes, need);
+  Ctx c;
+  ra_status s = make_ctx(stream, &c);
+  if (s != RA_OK) return s;
+  FfnArgs a;
+  a.B = batch;
+  a.L = seq;
+  a.Dm = model_dim;
+  a.F = ffn_dim;
+  a.chunk = chunk_size;
+  a.x = x;
+  a.w1 = w1;
+  a.b1 = b1;
+  a.w2 = w2;
+  a.b2 = b2;
+  a.out = out;
+  a.hidden = workspace;
+  uint64_t n = 0;
+  const char* why = nullptr;
+  cudaError_t e = launch_ffn(a, c, &n, &why);
+  g_launches += n;
+  if (why) return fail(RA_ERR_UNSUPPORTED, "%s", why);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "feed-forward launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 RA_API ra_status ra_sync_check(void* stream) {
   Ctx c;
   ra_status s = make_ctx(stream, &c);

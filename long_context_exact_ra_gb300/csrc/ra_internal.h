@@ -77,6 +77,20 @@ DecodeSplit decode_split(int B, int T, int S, int H, int num_shards);
 size_t decode_workspace_bytes(int B, int T, int S, int H, int D, int num_shards);
 cudaError_t launch_decode(const DecodeArgs& a, const Ctx& c, uint64_t* launches);
 
+// Blockwise feed-forward: out = max(0, x w1^T + b1) w2^T + b2, chunk by chunk.
+struct FfnArgs {
+  int B, L, Dm, F, chunk;
+  const void* x;    // [B, L, Dm] bf16
+  const void* w1;   // [F, Dm] bf16
+  const float* b1;  // [F] or nullptr
+  const void* w2;   // [Dm, F] bf16
+  const float* b2;  // [Dm] or nullptr
+  void* out;        // [B, L, Dm] bf16
+  void* hidden;     // [min(B*L, chunk), F] bf16 scratch
+};
+size_t ffn_workspace_bytes(long long rows, int chunk_size, int ffn_dim);
+cudaError_t launch_ffn(const FfnArgs& a, const Ctx& c, uint64_t* launches, const char** why);
+
 // Launchers.  Each returns the CUDA error of its launch(es) and adds the
 // number of kernels it launched to *launches.
 cudaError_t launch_fwd_f32(const FwdArgs& a, const Ctx& c, uint64_t* launches);

@@ -311,3 +311,60 @@ def make_decode_inputs(w: DecodeWorkload, cache_idx=None) -> DecodeInputs:
                 j = int(cache_idx[b]) + t
                 qseg[b, t] = kseg[b, min(max(j, 0), w.cache_len - 1)] if w.cache_len > 0 else 0
     return DecodeInputs(w, q, k, v, cache_idx, qseg, kseg)
+
+
+# ---------------------------------------------------------------------------
+# Blockwise feed-forward
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class FfnWorkload:
+    """x [B, L, Dm] through max(0, x w1^T + b1) w2^T + b2 in chunks of rows."""
+
+    name: str
+    batch: int
+    seq: int
+    model_dim: int
+    ffn_dim: int
+    chunk_size: int
+    seed: int = 0
+    bias: bool = True
+
+    def with_(self, **kw) -> "FfnWorkload":
+        d = dict(self.__dict__)
+        d.update(kw)
+        return FfnWorkload(**d)
+
+
+# The 7B shape (hidden 4096, feed-forward width 11008) on 16384 rows in two chunks.
+FFN_WORKLOADS = {
+    "7b": FfnWorkload("7B-shaped blockwise feed-forward B1 L16384 Dm4096 F11008 bf16, chunks of 8192 rows",
+                      1, 16384, 4096, 11008, 8192, seed=1007),
+}
+
+
+@dataclass
+class FfnInputs:
+    w: FfnWorkload
+    x: np.ndarray          # [B, L, Dm] bf16 bits
+    w1: np.ndarray         # [F, Dm] bf16 bits
+    b1: np.ndarray | None  # [F] float32
+    w2: np.ndarray         # [Dm, F] bf16 bits
+    b2: np.ndarray | None  # [Dm] float32
+
+    def as_f64(self, name: str) -> np.ndarray:
+        a = getattr(self, name)
+        if a is None:
+            return None
+        return bf16_bits_to_f32(a).astype(np.float64) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+def make_ffn_inputs(w: FfnWorkload) -> FfnInputs:
+    """x ~ N(0, 1); w1 ~ N(0, 1/Dm) and w2 ~ N(0, 1/F) (unit-variance pre-activations);
+    biases ~ 0.1 N(0, 1) in float32."""
+    x = tensor(w.seed, 0, (w.batch, w.seq, w.model_dim), 1.0, "bf16")
+    w1 = tensor(w.seed, 1, (w.ffn_dim, w.model_dim), 1.0 / np.sqrt(w.model_dim), "bf16")
+    w2 = tensor(w.seed, 2, (w.model_dim, w.ffn_dim), 1.0 / np.sqrt(w.ffn_dim), "bf16")
+    b1 = tensor(w.seed, 3, (w.ffn_dim,), 0.1, "f32") if w.bias else None
+    b2 = tensor(w.seed, 4, (w.model_dim,), 0.1, "f32") if w.bias else None
+    return FfnInputs(w, x, w1, b1, w2, b2)

@@ -21,7 +21,7 @@ _STATUS = {1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "device 
 
 EXPORTS = ("ra_fwd", "ra_bwd", "ra_bwd_workspace_size", "ra_sync_check", "ra_last_error",
            "ra_kernel_launches", "ra_selftest_timeout", "ra_bwd_noalloc", "ra_bwd_noalloc_max_scratch",
-           "ra_decode", "ra_decode_workspace_size")
+           "ra_decode", "ra_decode_workspace_size", "ra_blockwise_ffn", "ra_ffn_workspace_size")
 
 
 class RAError(RuntimeError):
@@ -66,6 +66,10 @@ def lib() -> ctypes.CDLL:
     L.ra_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     L.ra_decode.restype = i32
     L.ra_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.ra_ffn_workspace_size.restype = sz
+    L.ra_ffn_workspace_size.argtypes = [i32, i32, i32, i32]
+    L.ra_blockwise_ffn.restype = i32
+    L.ra_blockwise_ffn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp]
     _lib = L
     return L
 
@@ -225,6 +229,38 @@ def decode(q, k_cache, v_cache, cache_idx, q_segment_ids=None, kv_segment_ids=No
                            _dtype_code(q), _ptr(out), _ptr(lse), _ptr(workspace),
                            workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse
+
+
+def ffn_workspace_size(B, L, F, chunk_size) -> int:
+    return int(lib().ra_ffn_workspace_size(B, L, F, chunk_size))
+
+
+def blockwise_ffn(x, w1, b1, w2, b2, chunk_size, out=None, workspace=None, stream=None):
+    """ra_blockwise_ffn: max(0, x w1^T + b1) w2^T + b2 over x [B, L, Dm] bf16 in chunks of rows.
+
+    w1 [F, Dm] and w2 [Dm, F] bf16 (linear-layer layout); b1 [F], b2 [Dm] float32 or None."""
+    _check_tensor("x", x, dtype=torch.bfloat16)
+    B, L, Dm = x.shape
+    _check_tensor("w1", w1, dtype=torch.bfloat16)
+    _check_tensor("w2", w2, dtype=torch.bfloat16)
+    F = w1.shape[0]
+    if tuple(w1.shape) != (F, Dm) or tuple(w2.shape) != (Dm, F):
+        raise ValueError("w1 must be [F, Dm] and w2 [Dm, F]")
+    for name, t, n in (("b1", b1, F), ("b2", b2, Dm)):
+        if t is not None:
+            _check_tensor(name, t, dtype=torch.float32)
+            if tuple(t.shape) != (n,):
+                raise ValueError(f"{name} must have {n} entries")
+    if out is None:
+        out = torch.empty_like(x)
+    _check_tensor("out", out, x)
+    need = ffn_workspace_size(B, L, F, chunk_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _check(lib().ra_blockwise_ffn(_ptr(x), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2), B, L, Dm, F, int(chunk_size),
+                                  RA_BF16, _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
+    return out
 
 
 def sync_check(stream=None):

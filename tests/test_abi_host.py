@@ -114,3 +114,27 @@ def test_decode_validation_and_workspace(L):
     assert ws1 > 0 and ws2 >= 2 * ws1 - 512 and ws1 % 256 == 0
     assert L.ra_decode_workspace_size(1, 1, 0, 1, 64, 1, 1) == 0
     assert L.ra_decode_workspace_size(0, 1, 128, 1, 64, 1, 1) == 0
+
+
+def _ffn(L, x=16, w1=16, b1=None, w2=16, b2=None, B=1, S=256, Dm=64, F=128, chunk=128, dt=1, out=16, ws=16,
+         wsb=1 << 30):
+    P = lambda v: None if v is None else ctypes.c_void_p(v)
+    return L.ra_blockwise_ffn(P(x), P(w1), P(b1), P(w2), P(b2), B, S, Dm, F, chunk, dt, P(out), P(ws),
+                              ctypes.c_size_t(wsb), None)
+
+
+def test_ffn_validation_and_workspace(L):
+    assert _ffn(L, x=None) == ops.RA_ERR_INVALID_ARG and b"x is NULL" in L.ra_last_error()
+    assert _ffn(L, w2=24) == ops.RA_ERR_INVALID_ARG and b"16-byte" in L.ra_last_error()
+    assert _ffn(L, b1=20) == ops.RA_ERR_INVALID_ARG
+    assert _ffn(L, Dm=60) == ops.RA_ERR_INVALID_ARG  # not a multiple of 8
+    assert _ffn(L, F=100) == ops.RA_ERR_INVALID_ARG
+    assert _ffn(L, chunk=0) == ops.RA_ERR_INVALID_ARG
+    assert _ffn(L, B=0) == ops.RA_ERR_INVALID_ARG
+    assert _ffn(L, dt=0) == ops.RA_ERR_UNSUPPORTED
+    assert _ffn(L, wsb=100) == ops.RA_ERR_INVALID_ARG and b"workspace" in L.ra_last_error()
+    assert _ffn(L, S=0) == ops.RA_OK and L.ra_last_error() == b""
+    # one chunk of hidden activations: min(rows, chunk) x F bf16
+    assert L.ra_ffn_workspace_size(2, 1000, 128, 512) == 512 * 128 * 2
+    assert L.ra_ffn_workspace_size(1, 100, 128, 512) == 100 * 128 * 2
+    assert L.ra_ffn_workspace_size(0, 100, 128, 512) == 0
