@@ -501,6 +501,31 @@ def time_ffn(ops, torch, wf, iters, warmup, dev):
     return e0.elapsed_time(e1) / iters, flops
 
 
+def ffn_arm(args, peaks, peaks_src):
+    """--ffn-only: the blockwise feed-forward leg alone (profiling; rows = --seq, default 16384)."""
+    import torch
+
+    from long_context_exact_ra_gb300 import ops
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ops.lib()
+    wf = FFN_WORKLOADS["7b"]
+    if args.seq:
+        wf = wf.with_(name=f"{wf.name} at {args.seq} rows", seq=args.seq, chunk_size=min(wf.chunk_size, args.seq))
+    fms, ffl = time_ffn(ops, torch, wf, max(1, args.steps), max(1, args.warmup), dev)
+    tf = ffl / (fms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    print(json.dumps({"metric": "blockwise feed-forward TFLOP/s (ra_blockwise_ffn)", "value": round(tf, 1),
+                      "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": round(fms, 3), "higher_is_better": True, "dtype": "bf16",
+                      "data": "synthetic (seeded, no dataset)",
+                      "config": {"workload": wf.name, "note": "feed-forward leg alone, for profiling"},
+                      "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": UNIT,
+                                   "frac": round(tf / peak, 4), "peak_source": peaks_src,
+                                   "flops_per_launch": ffl}}), flush=True)
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_rows_rate(w, budget_s, x=None, start_rows=32):
     """Time the float64 oracle on sampled query rows of workload w; return
@@ -583,6 +608,8 @@ def main():
     ap.add_argument("--workload", type=int, choices=[2, 3, 4, 5], default=5)
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode leg (cache_len = --seq, default 131072); for profiling")
+    ap.add_argument("--ffn-only", action="store_true",
+                    help="time only the blockwise feed-forward leg (rows = --seq, default 16384); for profiling")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the seq-131072 forward, decode and feed-forward lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -597,6 +624,8 @@ def main():
         reference_arm(args)
     elif args.decode_only:
         decode_arm(args, peaks, src)
+    elif args.ffn_only:
+        ffn_arm(args, peaks, src)
     else:
         gpu_arm(args, peaks, src)
 
