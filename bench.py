@@ -439,6 +439,10 @@ def gpu_arm(args, peaks, peaks_src):
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+        if "decode_s131072" in result:
+            result["decode_s131072"]["cpu_baseline"] = cpu_baseline_decode(DECODE_WORKLOADS["7b"])
+        if "ffn_7b" in result:
+            result["ffn_7b"]["cpu_baseline"] = cpu_baseline_ffn(FFN_WORKLOADS["7b"])
     if args.seq:
         result["config"]["note"] = "reduced seq for profiling: not the benchmark workload"
     if ws > 1:
@@ -569,6 +573,54 @@ def cpu_baseline(w, budget_s=15.0):
             "sample": f"float64 oracle forward on {rows} sampled query rows of '{w.name}' "
                       f"(full key range per row, {secs:.1f} s); algorithmic FLOPs of the visible pairs; "
                       f"the backward is not sampled (same FLOP convention applies)"}
+
+
+def cpu_baseline_decode(wd, budget_s=5.0, cache_len=16384):
+    """The float64 decode oracle on one new token per sampled head against a cache of
+    `cache_len` entries (the decode workload's layout and distributions, a shorter
+    cache); reported as GB/s of K/V cache processed, the decode leg's unit."""
+    import oracle
+
+    from long_context_exact_ra_gb300.inputs import bf16_bits_to_f32, make_decode_inputs
+    w = wd.with_(cache_len=cache_len)
+    x = make_decode_inputs(w)
+    q = bf16_bits_to_f32(x.q).astype(np.float64)
+    g = np.random.Generator(np.random.PCG64(11))
+    t_sum, byts, rows = 0.0, 0, 0
+    while t_sum < budget_s:
+        h = int(g.integers(w.heads))
+        t0 = time.perf_counter()
+        oracle.ref_decode_rows(q, x.k_cache, x.v_cache, x.cache_idx, np.array([[0, h, 0]]), w.causal_block_size)
+        t_sum += time.perf_counter() - t0
+        byts += 2 * cache_len * w.head_dim * 2
+        rows += 1
+    return {"value": byts / t_sum / 1e9, "unit": "GB/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"float64 decode oracle on {rows} (head, token) rows against a {cache_len}-entry cache of "
+                      f"the same layout ({t_sum:.1f} s); bytes = the bf16 K/V rows each row reads"}
+
+
+def cpu_baseline_ffn(wf, budget_s=5.0):
+    """The float64 feed-forward oracle on sampled rows of the feed-forward workload (TFLOP/s)."""
+    import oracle
+
+    from long_context_exact_ra_gb300.inputs import make_ffn_inputs
+    xi = make_ffn_inputs(wf)
+    w1, w2 = xi.as_f64("w1"), xi.as_f64("w2")
+    b1 = xi.as_f64("b1") if xi.b1 is not None else np.zeros(wf.ffn_dim)
+    b2 = xi.as_f64("b2") if xi.b2 is not None else np.zeros(wf.model_dim)
+    xflat = xi.as_f64("x").reshape(-1, wf.model_dim)
+    g = np.random.Generator(np.random.PCG64(12))
+    t_sum, rows = 0.0, 0
+    while t_sum < budget_s:
+        r = g.integers(wf.batch * wf.seq, size=16)
+        xr = xflat[r]
+        t0 = time.perf_counter()
+        oracle.ffn_rows(xr, w1, b1, w2, b2)
+        t_sum += time.perf_counter() - t0
+        rows += len(r)
+    flops = 2.0 * 2 * rows * wf.model_dim * wf.ffn_dim
+    return {"value": flops / t_sum / 1e12, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"float64 feed-forward oracle on {rows} sampled rows of '{wf.name}' ({t_sum:.1f} s)"}
 
 
 def reference_arm(args):
