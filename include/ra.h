@@ -67,7 +67,7 @@ extern "C" {
 typedef enum {
   RA_OK = 0,
   RA_ERR_INVALID_ARG = 1,  /* bad pointer, shape, alignment or divisibility */
-  RA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement  */
+  RA_ERR_UNSUPPORTED = 2,  /* valid request this library does not implement */
   RA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed          */
   RA_ERR_TIMEOUT = 4       /* a bounded device-side wait ran out            */
 } ra_status;
