@@ -278,15 +278,14 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
             kmn = mn;
             kmx = mx;
           }
+          // Each lane classifies its own tile; the warp then walks the visible ones
+          // only, so skipped positions cost nothing serial.
           const int tend = min(32, P.tiles_per_shard - t0);
-          for (int tt = 0; tt < tend && alive; ++tt) {
-            const int t = t0 + tt;
-            const int ka = kbeg + t * kBN;
-            const int kvalid = min(kBN, kend - ka);
-            const int kb = ka + kvalid - 1;
-            const int tmn = __shfl_sync(0xffffffffu, kmn, tt);
-            const int tmx = __shfl_sync(0xffffffffu, kmx, tt);
-            int flags = 0;
+          int my_flags = kSkip0 | kSkip1;
+          if (lane < tend) {
+            const int ka = kbeg + my_t * kBN;
+            const int kb = ka + min(kBN, kend - ka) - 1;
+            my_flags = 0;
             for (int w = 0; w < 2; ++w) {
               const int qv = w == 0 ? qv0 : qv1;
               const int qa = q0 + w * kBM, ql = qa + qv - 1;
@@ -296,14 +295,21 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
                 else if (!(floordiv_pos(qa, c) >= floordiv_pos(kb, c))) full = false;
               }
               if (!skip && pb.seg) {
-                if (tmx < qmin[w] || tmn > qmax[w]) skip = true;
-                else if (!(qmin[w] == qmax[w] && tmn == qmax[w] && tmx == qmax[w])) full = false;
+                if (kmx < qmin[w] || kmn > qmax[w]) skip = true;
+                else if (!(qmin[w] == qmax[w] && kmn == qmax[w] && kmx == qmax[w])) full = false;
               }
-              if (kvalid < kBN) full = false;
-              if (skip) flags |= (w == 0 ? kSkip0 : kSkip1);
-              else if (!full) flags |= (w == 0 ? kMask0 : kMask1);
+              if (kb - ka + 1 < kBN) full = false;
+              if (skip) my_flags |= (w == 0 ? kSkip0 : kSkip1);
+              else if (!full) my_flags |= (w == 0 ? kMask0 : kMask1);
             }
-            if ((flags & (kSkip0 | kSkip1)) == (kSkip0 | kSkip1)) continue;
+          }
+          uint32_t todo = __ballot_sync(0xffffffffu, (my_flags & (kSkip0 | kSkip1)) != (kSkip0 | kSkip1));
+          while (todo != 0u && alive) {
+            const int tt = __ffs(todo) - 1;
+            todo &= todo - 1u;
+            const int flags = __shfl_sync(0xffffffffu, my_flags, tt);
+            const int ka = kbeg + (t0 + tt) * kBN;
+            const int kvalid = min(kBN, kend - ka);
             if (lane == 0) {
               Rec r;
               r.kind = kRecTile;
