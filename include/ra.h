@@ -77,6 +77,12 @@ typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
 /*
  * Forward: out, lse <- attention(q, k, v).
  * One persistent kernel launch for RA_BF16; one launch for RA_F32.
+ * RA_BF16 outside stream capture: before the launch the call takes a 16-byte
+ * unit counter from a stream-ordered memory pool of the library's own (created
+ * on the device's first call, memory kept between calls), zeroes it on
+ * `stream` and frees it on `stream` after the launch, so that the kernel's
+ * CTAs take query-tile units as they free up.  Under stream capture it uses a
+ * fixed schedule instead; both give bit-identical results.
  */
 ra_status ra_fwd(const void* q, const void* k, const void* v,
                  const int32_t* segment_ids, int causal_block_size,

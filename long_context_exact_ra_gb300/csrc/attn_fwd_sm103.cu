@@ -28,6 +28,7 @@
 // stay <= 256.  Every mbarrier wait is bounded (see sm103.cuh).
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <cudaTypedefs.h>
 
 #include "ra_internal.h"
@@ -103,6 +104,8 @@ struct FwdParams {
   int pairs_per_shard;  // ceil(tiles_per_shard / 2)
   int num_units;        // B * H * N * pairs_per_shard
   float scale_log2;     // log2(e) / sqrt(D)
+  int* unit_counter;    // zeroed per call: CTAs draw tickets as they free up; null: static pairs
+  int group_heads;      // (b, h) heads per ticket group (their K and V fit in part of L2)
 };
 
 __device__ __forceinline__ int floordiv_pos(int a, int c) { return a / c; }  // a >= 0
@@ -120,6 +123,22 @@ __device__ __forceinline__ void unit_coords(const FwdParams& P, int u, int& b, i
   pr = g % P.pairs_per_shard;
   b = bh / P.p.H;
   h = bh % P.p.H;
+}
+
+// Ticket t -> unit.  The (b, h) heads form groups of group_heads whose K and V
+// fit in L2 together; a group's tickets go rank-major (the longest causal unit of
+// every head of the group, then the next longest, ...), so the last tickets of a
+// group are its shortest units and the CTAs finish together.
+__device__ __forceinline__ int ticket_unit(const FwdParams& P, int t) {
+  const int per_head = P.p.N * P.pairs_per_shard;
+  const int bh_total = P.p.B * P.p.H;
+  const int G = P.group_heads;
+  const int g = t / (G * per_head);
+  const int g0 = g * G;                     // first head of the group
+  const int gh = min(G, bh_total - g0);     // heads in the group (the last may be short)
+  const int w = t - g * G * per_head;       // ticket within the group, < gh * per_head
+  const int rank = w / gh;                  // 0 = longest causal work
+  return (g0 + (w - rank * gh)) * per_head + rank;
 }
 
 template <int D>
@@ -191,19 +210,42 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
       ++rec_n;
       return true;
     };
-    // Units go out in balanced pairs: within a head, unit r (long causal work)
-    // with unit per_head - 1 - r (short), so every CTA's step takes about the same
-    // time and all CTAs move through one or two heads together, keeping those
-    // heads' operands resident in L2.
+    // Unit order.  With a unit counter, CTAs draw tickets (ticket_unit: L2-sized head
+    // groups, longest units first) as they become free, so uneven unit costs
+    // (packed documents, few units per SM) even out; the next ticket is drawn one
+    // unit ahead so its latency hides behind the current unit.  Without one,
+    // units go out in balanced pairs: within a head, unit r (long causal work) with
+    // unit per_head - 1 - r (short), CTA c taking pairs c, c + G, ...  Either way all
+    // CTAs move through one or two heads together, keeping those heads' operands
+    // resident in L2.
     const int per_head = pb.N * P.pairs_per_shard;
     const int pairs_per_head = (per_head + 1) / 2;
     const int num_super = (P.num_units / per_head) * pairs_per_head;
-    for (int su = blockIdx.x; su < num_super && alive; su += gridDim.x)
-     for (int half = 0; half < 2 && alive; ++half) {
-      const int rr = su % pairs_per_head;
-      const int rank = half == 0 ? rr : per_head - 1 - rr;
-      if (half == 1 && rank == rr) continue;  // odd count: the middle unit has no partner
-      const int u = (su / pairs_per_head) * per_head + rank;
+    int st_su = blockIdx.x, st_half = 0;
+    auto static_next = [&]() -> int {
+      while (st_su < num_super) {
+        const int su = st_su, half = st_half;
+        if (++st_half == 2) {
+          st_half = 0;
+          st_su += gridDim.x;
+        }
+        const int rr = su % pairs_per_head;
+        const int rank = half == 0 ? rr : per_head - 1 - rr;
+        if (half == 1 && rank == rr) continue;  // odd count: the middle unit has no partner
+        return (su / pairs_per_head) * per_head + rank;
+      }
+      return -1;
+    };
+    auto ticket = [&]() -> int {  // lane 0 draws, the warp gets the unit (or -1)
+      int t = 0;
+      if (lane == 0) t = atomicAdd(P.unit_counter, 1);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      return t < P.num_units ? ticket_unit(P, t) : -1;
+    };
+    int u = P.unit_counter ? ticket() : static_next();
+    while (u >= 0 && alive) {
+      int ahead = 0;
+      if (P.unit_counter && lane == 0) ahead = atomicAdd(P.unit_counter, 1);
       int b, h, j, pr;
       unit_coords(P, u, b, h, j, pr);
       const int shard0 = j * pb.Ssh;
@@ -357,6 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
       }
       alive = __shfl_sync(0xffffffffu, alive, 0);
       ++unit_n;
+      if (P.unit_counter) {
+        const int t = __shfl_sync(0xffffffffu, ahead, 0);
+        u = t < P.num_units ? ticket_unit(P, t) : -1;
+      } else {
+        u = static_next();
+      }
     }
     if (lane == 0 && alive) {
       Rec r;
@@ -705,6 +753,52 @@ bool make_tile_map(CUtensorMap* m, const void* ptr, const Problem& p, int rows) 
   return r == CUDA_SUCCESS;
 }
 
+// A zeroed 4-byte counter for one call, or null (stream capture, or no pool).
+static int* take_unit_counter(const Ctx& c) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[256];
+  static bool tried[256];
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(c.stream, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (cs != cudaStreamCaptureStatusNone || c.device < 0 || c.device >= 256) return nullptr;
+  cudaMemPool_t pool = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!tried[c.device]) {
+      tried[c.device] = true;
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.handleTypes = cudaMemHandleTypeNone;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = c.device;
+      if (cudaMemPoolCreate(&pools[c.device], &props) == cudaSuccess) {
+        uint64_t keep = UINT64_MAX;  // keep the pool's few bytes reserved between calls
+        cudaMemPoolSetAttribute(pools[c.device], cudaMemPoolAttrReleaseThreshold, &keep);
+      } else {
+        pools[c.device] = nullptr;
+      }
+      (void)cudaGetLastError();
+    }
+    pool = pools[c.device];
+  }
+  if (!pool) return nullptr;
+  void* p = nullptr;
+  if (cudaMallocFromPoolAsync(&p, 16, pool, c.stream) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (cudaMemsetAsync(p, 0, 16, c.stream) != cudaSuccess) {
+    (void)cudaGetLastError();
+    cudaFreeAsync(p, c.stream);
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<int*>(p);
+}
+
 template <int D>
 static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
   using Cf = Cfg<D>;
@@ -734,10 +828,24 @@ static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* l
   }
   const int per_head = p.N * P.pairs_per_shard;
   const int num_super = (P.num_units / per_head) * ((per_head + 1) / 2);  // balanced unit pairs
-  const int grid = std::min(c.num_sms, num_super);
+  // A unit counter of this call's own, from a stream-ordered pool on the caller's
+  // stream, so that calls running at the same time never share one.  Under stream
+  // capture the static pairs are used instead (same results: each unit is computed
+  // whole by one CTA either way).
+  P.unit_counter = take_unit_counter(c);
+  {  // heads whose K and V (2 * S * D bf16 each) fit in 48 MB of L2 together
+    const long long kv = 2LL * p.S * p.D * 2;
+    P.group_heads = (int)std::max(1LL, std::min((long long)p.B * p.H, (48LL << 20) / kv));
+  }
+  const int grid = std::min(c.num_sms, P.unit_counter ? P.num_units : num_super);
   fwd_bf16_kernel<D><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, P);
   *launches += 1;
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (P.unit_counter) {
+    cudaError_t ef = cudaFreeAsync(P.unit_counter, c.stream);
+    if (e == cudaSuccess) e = ef;
+  }
+  return e;
 }
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
