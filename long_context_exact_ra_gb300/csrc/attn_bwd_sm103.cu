@@ -110,6 +110,8 @@ struct BwdParams {
   int num_units;
   float scale;       // 1 / sqrt(D)
   float scale_log2;  // log2(e) / sqrt(D)
+  int* unit_counter; // zeroed by the preprocess kernel: CTAs draw tickets as they free up
+  int group_heads;   // (b, h) heads per ticket group (their Q, dO, dQ accumulator fit in part of L2)
 };
 
 __device__ __forceinline__ void red_add_v2(float* addr, float a, float b) {
@@ -126,7 +128,9 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 // ---------------------------------------------------------------------------
 __global__ void bwd_pre_kernel(Problem p, const __nv_bfloat16* __restrict__ out,
                                const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
-                               float2* __restrict__ ld2, int Sp, float* __restrict__ dq_accum) {
+                               float2* __restrict__ ld2, int Sp, float* __restrict__ dq_accum,
+                               int* __restrict__ unit_counter) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *unit_counter = 0;
   const int warps = blockDim.x / 32;
   const long long row = (long long)blockIdx.x * warps + threadIdx.x / 32;  // (b, s, h) row
   const int lane = threadIdx.x & 31;
@@ -180,6 +184,22 @@ __device__ __forceinline__ void bunit_coords(const BwdParams& P, int u, int& b, 
   t = rank % P.tiles_per_shard;
   b = bh / P.p.H;
   h = bh % P.p.H;
+}
+
+// Ticket t -> unit.  The (b, h) heads form groups of group_heads whose Q, dO and
+// dQ accumulator fit in L2 together; a group's tickets go rank-major (key tile 0
+// of every head of the group, the longest causal work, then key tile 1, ...), so
+// the last tickets of a group are its shortest units and the CTAs finish together.
+__device__ __forceinline__ int bticket_unit(const BwdParams& P, int t) {
+  const int per_head = P.p.N * P.tiles_per_shard;
+  const int bh_total = P.p.B * P.p.H;
+  const int G = P.group_heads;
+  const int g = t / (G * per_head);
+  const int g0 = g * G;
+  const int gh = min(G, bh_total - g0);
+  const int w = t - g * G * per_head;
+  const int rank = w / gh;
+  return (g0 + (w - rank * gh)) * per_head + rank;
 }
 
 // ---------------------------------------------------------------------------
@@ -254,19 +274,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++rec_n;
       return true;
     };
-    // Units go out in balanced pairs: within a head, unit r (long causal work)
-    // with unit per_head - 1 - r (short), so every CTA's step takes about the same
-    // time and all CTAs move through one or two heads together, keeping those
-    // heads' operands resident in L2.
-    const int per_head = pb.N * P.tiles_per_shard;
-    const int pairs_per_head = (per_head + 1) / 2;
-    const int num_super = (P.num_units / per_head) * pairs_per_head;
-    for (int su = blockIdx.x; su < num_super && alive; su += gridDim.x)
-     for (int half = 0; half < 2 && alive; ++half) {
-      const int rr = su % pairs_per_head;
-      const int rank = half == 0 ? rr : per_head - 1 - rr;
-      if (half == 1 && rank == rr) continue;  // odd count: the middle unit has no partner
-      const int u = (su / pairs_per_head) * per_head + rank;
+    // CTAs draw tickets (bticket_unit: L2-sized head groups, longest units first)
+    // as they become free, so uneven unit costs even out and all CTAs move through
+    // one group of heads together; the next ticket is drawn one unit ahead so its
+    // latency hides behind the current unit.
+    auto ticket = [&]() -> int {  // lane 0 draws, the warp gets the unit (or -1)
+      int tk = 0;
+      if (lane == 0) tk = atomicAdd(P.unit_counter, 1);
+      tk = __shfl_sync(0xffffffffu, tk, 0);
+      return tk < P.num_units ? bticket_unit(P, tk) : -1;
+    };
+    int u = ticket();
+    while (u >= 0 && alive) {
+      int ahead = 0;
+      if (lane == 0) ahead = atomicAdd(P.unit_counter, 1);
       int b, h, k, t;
       bunit_coords(P, u, b, h, k, t);
       const int k0 = k * pb.Ssh + t * kT;
@@ -383,6 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       alive = __shfl_sync(0xffffffffu, alive, 0);
       ++unit_n;
+      const int tk = __shfl_sync(0xffffffffu, ahead, 0);
+      u = tk < P.num_units ? bticket_unit(P, tk) : -1;
     }
     if (lane == 0 && alive) {
       BRec r;
@@ -714,7 +737,8 @@ static cudaError_t launch_bwd_bf16_d(const BwdArgs& a, const Ctx& c, uint64_t* l
   const long long rows = (long long)p.B * p.S * p.H;
   const int Sp = bwd_row_pitch(p.S);
   bwd_pre_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, c.stream>>>(
-      p, (const __nv_bfloat16*)a.out, (const __nv_bfloat16*)a.dout, a.lse, (float2*)a.delta, Sp, a.dq_accum);
+      p, (const __nv_bfloat16*)a.out, (const __nv_bfloat16*)a.dout, a.lse, (float2*)a.delta, Sp, a.dq_accum,
+      a.unit_counter);
   *launches += 1;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -731,6 +755,11 @@ static cudaError_t launch_bwd_bf16_d(const BwdArgs& a, const Ctx& c, uint64_t* l
   P.num_units = p.B * p.H * p.N * P.tiles_per_shard;
   P.scale = (float)(1.0 / sqrt((double)p.D));
   P.scale_log2 = (float)(1.4426950408889634 / sqrt((double)p.D));
+  P.unit_counter = a.unit_counter;
+  {  // heads whose Q, dO (bf16) and dQ accumulator (fp32), 8 * S * D bytes, fit in 48 MB of L2
+    const long long per = 8LL * p.S * p.D;
+    P.group_heads = (int)std::max(1LL, std::min((long long)p.B * p.H, (48LL << 20) / per));
+  }
   static bool attr_set[256][2];
   const int di = D == 64 ? 0 : 1;
   if (!attr_set[c.device][di]) {
@@ -738,9 +767,7 @@ static cudaError_t launch_bwd_bf16_d(const BwdArgs& a, const Ctx& c, uint64_t* l
     if (e != cudaSuccess) return e;
     attr_set[c.device][di] = true;
   }
-  const int per_head = p.N * P.tiles_per_shard;
-  const int num_super = (P.num_units / per_head) * ((per_head + 1) / 2);  // balanced unit pairs
-  const int grid = std::min(c.num_sms, num_super);
+  const int grid = std::min(c.num_sms, P.num_units);
   bwd_bf16_kernel<D><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, mdo, P);
   *launches += 1;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

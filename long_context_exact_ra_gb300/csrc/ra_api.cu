@@ -200,6 +200,7 @@ RA_API ra_status ra_bwd(const void* q, const void* k, const void* v, const void*
   } else {
     a.dq_accum = (float*)workspace;
     a.delta = (float*)((char*)workspace + bwd_delta_offset(batch, seq, heads, head_dim));
+    a.unit_counter = (int*)((char*)workspace + bwd_counter_offset(batch, seq, heads, head_dim));
     e = launch_bwd_bf16(a, c, &n, &why);
   }
   g_launches += n;

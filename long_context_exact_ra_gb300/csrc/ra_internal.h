@@ -40,6 +40,7 @@ struct BwdArgs {
   void* dv;
   float* dq_accum;  // [B, S, H, D] fp32 scratch (bf16 path)
   float* delta;     // fp32 path: [B, H, S] Delta; bf16 path: float2 (lse*log2(e), Delta) rows of bwd_row_pitch
+  int* unit_counter;  // bf16 path: the main kernel's unit counter (in the workspace)
 };
 
 // Launch context: device facts and the device status word.
@@ -105,16 +106,19 @@ ra_status set_last_error(ra_status s, const char* msg);
 // Scratch layout of the bf16 backward (byte offsets into the caller's workspace):
 // the fp32 dQ accumulator, then (lse*log2(e), Delta) float2 pairs per (b, h) row
 // with an even row pitch (16-byte aligned pairs of entries) and a tail pad so
-// that a 130-entry bulk copy starting at any even index stays inside.
+// that a 130-entry bulk copy starting at any even index stays inside ...
 constexpr int kBwdVecEntries = 130;
 inline int bwd_row_pitch(int S) { return S + (S & 1); }
 inline size_t bwd_delta_offset(int B, int S, int H, int D) {
   size_t dq = (size_t)B * S * H * D * sizeof(float);
   return (dq + 255) & ~(size_t)255;
 }
-inline size_t bwd_workspace_bytes(int B, int S, int H, int D) {
+// ... and last a 256-byte slot whose first word is the main kernel's unit counter
+// (zeroed by the preprocess kernel).
+inline size_t bwd_counter_offset(int B, int S, int H, int D) {
   const size_t vec = ((size_t)B * H * bwd_row_pitch(S) + kBwdVecEntries) * 2 * sizeof(float);
   return bwd_delta_offset(B, S, H, D) + ((vec + 255) & ~(size_t)255);
 }
+inline size_t bwd_workspace_bytes(int B, int S, int H, int D) { return bwd_counter_offset(B, S, H, D) + 256; }
 
 }  // namespace ra
