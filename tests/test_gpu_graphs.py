@@ -2,7 +2,12 @@
 they can be captured into a CUDA graph and replayed.  Checks: forward + backward
 captured once and replayed on new input values give the eager results, and a
 captured decode step follows a cache index that changes in device memory
-between replays (the decode loop needs no host round trip)."""
+between replays (the decode loop needs no host round trip).
+
+The bf16 forward draws its units from a per-call counter when called eagerly
+and uses a fixed schedule under capture: both must give bit-identical results
+(packed documents, several L2 head groups with a short last one, ragged
+shards), and calls in flight on two streams at once must not share a counter."""
 import numpy as np
 import pytest
 import torch
@@ -90,3 +95,72 @@ def test_decode_graph_follows_the_device_cache_index():
         assert torch.equal(got[0], out) and torch.equal(got[1], lse), new
     # the last indices leave one and two visible keys: every token still sees a key
     assert np.isfinite(lse.cpu().numpy()).all()
+
+
+def _fwd_static_and_dynamic(q, k, v, seg, c, N):
+    """The forward captured in a graph (fixed unit schedule) and called eagerly
+    (units drawn from a per-call counter)."""
+    B, S, H, D = q.shape
+    out_g, lse_g = torch.empty_like(q), torch.empty(B, H, S, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ops.fwd(q, k, v, seg, c, N, out=out_g, lse=lse_g)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ops.fwd(q, k, v, seg, c, N, out=out_g, lse=lse_g)
+    graph.replay()
+    torch.cuda.synchronize()
+    out_e, lse_e = ops.fwd(q, k, v, seg, c, N)
+    ops.sync_check()
+    return (out_g, lse_g), (out_e, lse_e)
+
+
+@pytest.mark.parametrize("B,S,H,D,N,c,docs", [
+    (3, 1536, 5, 64, 3, 1, True),      # packed documents, one head group, units of uneven cost
+    (2, 32768, 2, 128, 4, 1, False),   # 16 MB of K/V per head: groups of 3 heads, the last one short
+    (1, 1000, 3, 128, 2, 0, False),    # ragged shards, non-causal
+])
+def test_forward_unit_schedule_does_not_change_results(B, S, H, D, N, c, docs):
+    q, k, v = (torch.empty(B, S, H, D, dtype=torch.bfloat16, device="cuda") for _ in range(3))
+    for i, t in enumerate((q, k, v)):
+        _fill(t, 300 + i)
+    seg = None
+    if docs:
+        g = np.random.Generator(np.random.PCG64(7))
+        ids = np.zeros((B, S), dtype=np.int32)
+        for b in range(B):
+            pos, doc = 0, 0
+            while pos < S:
+                n = int(g.integers(1, 400))
+                ids[b, pos:pos + n] = doc
+                pos, doc = pos + n, doc + 1
+        seg = torch.from_numpy(ids).cuda()
+    (og, lg), (oe, le) = _fwd_static_and_dynamic(q, k, v, seg, c, N)
+    assert torch.equal(og, oe) and torch.equal(lg, le)
+
+
+def test_concurrent_forward_calls_use_separate_counters():
+    B, S, H, D, N = 2, 4096, 4, 128, 4
+    inputs = []
+    for j in range(2):
+        t = [torch.empty(B, S, H, D, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+        for i, x in enumerate(t):
+            _fill(x, 500 + 10 * j + i)
+        inputs.append(t)
+    ref = [ops.fwd(*t, None, 1, N) for t in inputs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    got = [[None, None] for _ in range(2)]
+    for rep in range(3):  # several rounds of two calls in flight on two streams
+        for j, s in enumerate(streams):
+            with torch.cuda.stream(s):
+                got[j] = ops.fwd(*inputs[j], None, 1, N, stream=s)
+    torch.cuda.synchronize()
+    ops.sync_check()
+    for (o, l), (ro, rl) in zip(got, ref):
+        assert torch.equal(o, ro) and torch.equal(l, rl)
