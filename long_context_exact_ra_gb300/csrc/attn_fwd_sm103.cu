@@ -46,7 +46,7 @@ constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum : int { kRecTile = 0, kRecUnitEnd = 1, kRecStop = 2 };
-enum : int { kSkip0 = 1, kSkip1 = 2, kMask0 = 4, kMask1 = 8 };
+enum : int { kSkip0 = 1, kSkip1 = 2, kMask0 = 4, kMask1 = 8, kKeyUni = 16 };  // kKeyUni: every key id of the tile is kseg
 
 struct __align__(16) Rec {
   int kind;
@@ -56,7 +56,8 @@ struct __align__(16) Rec {
   int b, h;
   int q0;       // first row of Q tile 0 (global); tile 1 starts at q0 + 128
   int qvalid0, qvalid1;  // rows of each Q tile inside the shard (0 = tile absent)
-  int pad[3];
+  int kseg;              // with kKeyUni: the segment id of every key of the tile
+  int pad[2];
 };
 
 template <int D>
@@ -344,12 +345,17 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
               if (skip) my_flags |= (w == 0 ? kSkip0 : kSkip1);
               else if (!full) my_flags |= (w == 0 ? kMask0 : kMask1);
             }
+            if constexpr (D == 64) {  // a masked row then needs one id compare (see the softmax)
+              if (pb.seg && kmn == kmx) my_flags |= kKeyUni;
+            }
           }
           uint32_t todo = __ballot_sync(0xffffffffu, (my_flags & (kSkip0 | kSkip1)) != (kSkip0 | kSkip1));
           while (todo != 0u && alive) {
             const int tt = __ffs(todo) - 1;
             todo &= todo - 1u;
             const int flags = __shfl_sync(0xffffffffu, my_flags, tt);
+            int kseg = 0;
+            if constexpr (D == 64) kseg = __shfl_sync(0xffffffffu, kmn, tt);
             const int ka = kbeg + (t0 + tt) * kBN;
             const int kvalid = min(kBN, kend - ka);
             if (lane == 0) {
@@ -363,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
               r.q0 = q0;
               r.qvalid0 = qv0;
               r.qvalid1 = qv1;
+              if constexpr (D == 64) r.kseg = kseg;
               alive = publish(r);
               const int s = tile_n % C::KST;
               const uint32_t par = ((tile_n / C::KST) & 1) ^ 1;
@@ -593,8 +600,17 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
           // block of key kstart + x must not exceed the row's block
           long long lim = r.kvalid;
           if (pb.causal > 0) lim = min(lim, ((long long)qrow / pb.causal + 1) * pb.causal - r.kstart);
-          const int nvis = (int)max(lim, 0LL);
-          if (pb.seg) {
+          int nvis = (int)max(lim, 0LL);
+          // With one segment id across the tile's keys (packed documents: the causal
+          // diagonal tiles), a row sees all of the tile or none of it, and the 128 key
+          // ids need not be read.  Only at D = 64: at D = 128 the extra branch in this
+          // 168-register kernel cost ~1 % of the unmasked forward.
+          bool uni = false;
+          if constexpr (D == 64) uni = pb.seg != nullptr && (r.flags & kKeyUni) != 0;
+          if (uni) {
+            if (__ldg(pb.seg + (size_t)r.b * pb.S + min(qrow, pb.S - 1)) != r.kseg) nvis = 0;
+          }
+          if (pb.seg && !uni) {
             const int* ks = pb.seg + (size_t)r.b * pb.S + r.kstart;
             const int qseg = __ldg(pb.seg + (size_t)r.b * pb.S + min(qrow, pb.S - 1));
             if (r.kvalid == 128 && ((reinterpret_cast<uintptr_t>(ks) & 15u) == 0)) {
