@@ -10,9 +10,11 @@
 //   dS = P * (dO V^T - Delta),  dK = dS^T Q / sqrt(d),  dQ = dS K / sqrt(d).
 //
 // Three launches:
-//   1. preprocess: Delta = rowsum(dO * O) next to lse * log2(e); zero the fp32 dQ accumulator
+//   1. preprocess: Delta = rowsum(dO * O) next to lse * log2(e); zero the fp32 dQ
+//      accumulator and the main kernel's unit counter
 //   2. main (persistent, one CTA per SM, 10 warps): one unit = one 128-key
-//      K/V tile of one (batch, head).  The unit visits the query tiles in the
+//      K/V tile of one (batch, head); CTAs draw units from the counter as they
+//      free up.  The unit visits the query tiles in the
 //      order the key block travels around the ring: query shards j = k, k+1,
 //      ... (mod N) ("Ring Attention with Blockwise Transformers for
 //      Near-Infinite Context", paper review page, 环形注意力算法), skipping
@@ -174,9 +176,9 @@ __global__ void bwd_fin_kernel(size_t n4, const float4* __restrict__ acc, uint2*
   }
 }
 
-// Unit u -> (b, h, key shard k, tile t).  Head-major, so the head's Q, dO and
-// fp32 dQ accumulator stay resident in L2 while its key tiles are processed;
-// within a head key tiles go by increasing position (longest causal work first).
+// Unit u -> (b, h, key shard k, tile t).  Units are numbered head-major, and
+// within a head by increasing key position (rank 0 = longest causal work); the
+// order in which CTAs take them is set by bticket_unit.
 __device__ __forceinline__ void bunit_coords(const BwdParams& P, int u, int& b, int& h, int& k, int& t) {
   const int per_head = P.p.N * P.tiles_per_shard;
   const int bh = u / per_head, rank = u % per_head;

@@ -13,9 +13,11 @@
 // How (one persistent CTA per SM, 10 warps):
 //   warps 0-3  softmax warpgroup for Q tile 0 (TMEM lanes 0-127, one row per thread)
 //   warps 4-7  softmax warpgroup for Q tile 1
-//   warp 8     producer: walks the ring schedule, classifies each 128-key tile
-//              (skip / full / needs a mask), publishes a record per visible
-//              tile and TMA-loads K and V into a smem ring (128B swizzle)
+//   warp 8     producer: takes query-tile-pair units (from a per-call counter,
+//              or a fixed schedule under stream capture), walks the ring
+//              schedule, classifies 32 key tiles at once (one per lane: skip /
+//              full / needs a mask), publishes a record per visible tile and
+//              TMA-loads K and V into a smem ring (128B swizzle)
 //   warp 9     MMA issuer: S_w = Q_w K^T (SS, fp32 in TMEM), then
 //              O_w += P_w V with P_w read from TMEM (TS), ping-ponging the two
 //              Q tiles so the tensor pipe runs one tile's MMAs while the other
@@ -111,11 +113,10 @@ struct FwdParams {
 
 __device__ __forceinline__ int floordiv_pos(int a, int c) { return a / c; }  // a >= 0
 
-// Unit u -> (b, h, query shard j, pair index).  Units are head-major: all CTAs
-// work on one or two heads at a time, so that head's K and V stay resident in
-// L2 while every query tile of the head streams over them.  Within a head the
-// query tiles go by decreasing position (longest causal work first); CTA c
-// takes units c, c + G, c + 2G, ...
+// Unit u -> (b, h, query shard j, pair index).  Units are numbered head-major,
+// and within a head by decreasing query position (rank 0 = longest causal work).
+// The order in which CTAs take them is set by ticket_unit (dynamic) or by the
+// static pairs in the producer.
 __device__ __forceinline__ void unit_coords(const FwdParams& P, int u, int& b, int& h, int& j, int& pr) {
   const int per_head = P.p.N * P.pairs_per_shard;
   const int bh = u / per_head;
