@@ -25,7 +25,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import re
 import statistics
@@ -40,8 +39,7 @@ sys.path.insert(0, ROOT)
 
 from long_context_exact_ra_gb300 import flops as F  # noqa: E402
 from long_context_exact_ra_gb300.inputs import (DECODE_WORKLOADS, FFN_WORKLOADS, WORKLOADS,  # noqa: E402
-                                                decode_cache_idx, make_ffn_inputs, make_inputs, sample_rows,
-                                                tensor)
+                                                decode_cache_idx, make_ffn_inputs, make_inputs, tensor)
 
 METRIC = "attention TFLOP/s (causal bf16 fwd/bwd, 1xGB300) and % of dense BF16 tensor peak"
 UNIT = "TFLOP/s"

@@ -8,7 +8,6 @@ import sys
 from contextlib import redirect_stdout
 
 import pytest
-import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
