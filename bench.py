@@ -529,6 +529,42 @@ def ffn_arm(args, peaks, peaks_src):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
+def blas_threads():
+    """Threads numpy's BLAS (which runs the oracle's float64 products) uses: from
+    threadpoolctl when installed, else from the OpenBLAS query function of the
+    library numpy ships; None when neither is available."""
+    try:
+        import threadpoolctl
+        for info in threadpoolctl.threadpool_info():
+            if info.get("user_api") == "blas":
+                return int(info["num_threads"])
+    except Exception:
+        pass
+    import ctypes
+    import glob
+    libdir = os.path.join(os.path.dirname(np.__file__), os.pardir, "numpy.libs")
+    for path in sorted(glob.glob(os.path.join(libdir, "*openblas*"))):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for name in ("scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads",
+                     "openblas_get_num_threads64_", "openblas_get_num_threads"):
+            fn = getattr(lib, name, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn())
+    return None
+
+
+def oracle_threads():
+    """(cores the oracle runs on, BLAS threads or None): the BLAS thread count
+    capped by the CPUs this process may use."""
+    cpus = len(os.sched_getaffinity(0))
+    bt = blas_threads()
+    return (min(cpus, bt) if bt else cpus), bt
+
+
 def oracle_rows_rate(w, budget_s, x=None, start_rows=32):
     """Time the float64 oracle on sampled query rows of workload w; return
     (algorithmic TFLOP/s, rows, seconds, cores)."""
@@ -562,12 +598,12 @@ def oracle_rows_rate(w, budget_s, x=None, start_rows=32):
             total_f += 4.0 * w.head_dim * w.seq * n
         total_rows += n
         n = min(n * 2, 4096)
-    return total_f / total_t / 1e12, total_rows, total_t, len(os.sched_getaffinity(0))
+    return total_f / total_t / 1e12, total_rows, total_t, oracle_threads()[0]
 
 
 def cpu_baseline(w, budget_s=15.0):
     tf, rows, secs, cores = oracle_rows_rate(w, budget_s)
-    return {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": tf, "unit": UNIT, "cores": cores, "blas_threads": oracle_threads()[1], "kind": "oracle",
             "sample": f"float64 oracle forward on {rows} sampled query rows of '{w.name}' "
                       f"(full key range per row, {secs:.1f} s); algorithmic FLOPs of the visible pairs; "
                       f"the backward is not sampled (same FLOP convention applies)"}
@@ -592,7 +628,8 @@ def cpu_baseline_decode(wd, budget_s=5.0, cache_len=16384):
         t_sum += time.perf_counter() - t0
         byts += 2 * cache_len * w.head_dim * 2
         rows += 1
-    return {"value": byts / t_sum / 1e9, "unit": "GB/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+    cores, bt = oracle_threads()
+    return {"value": byts / t_sum / 1e9, "unit": "GB/s", "cores": cores, "blas_threads": bt, "kind": "oracle",
             "sample": f"float64 decode oracle on {rows} (head, token) rows against a {cache_len}-entry cache of "
                       f"the same layout ({t_sum:.1f} s); bytes = the bf16 K/V rows each row reads"}
 
@@ -617,7 +654,8 @@ def cpu_baseline_ffn(wf, budget_s=5.0):
         t_sum += time.perf_counter() - t0
         rows += len(r)
     flops = 2.0 * 2 * rows * wf.model_dim * wf.ffn_dim
-    return {"value": flops / t_sum / 1e12, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+    cores, bt = oracle_threads()
+    return {"value": flops / t_sum / 1e12, "unit": UNIT, "cores": cores, "blas_threads": bt, "kind": "oracle",
             "sample": f"float64 feed-forward oracle on {rows} sampled rows of '{wf.name}' ({t_sum:.1f} s)"}
 
 
@@ -643,6 +681,7 @@ def reference_arm(args):
            "config": {"workload": w.name, "batch": w.batch, "seq": w.seq, "heads": w.heads,
                       "head_dim": w.head_dim, "num_shards": w.num_shards},
            "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": cores,
+                            "blas_threads": oracle_threads()[1],
                             "sample": f"each step: float64 oracle forward on sampled query rows for "
                                       f"~{per_step:.0f} s"},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
