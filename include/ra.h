@@ -92,8 +92,9 @@ ra_status ra_fwd(const void* q, const void* k, const void* v,
 
 /*
  * Bytes of device scratch that ra_bwd needs for this shape (float32 dQ
- * accumulator and the per-row Delta = rowsum(dO * out)).  The caller
- * allocates it; its contents on entry do not matter.
+ * accumulator, the per-row Delta = rowsum(dO * out), and for RA_BF16 the main
+ * kernel's unit counter).  The caller allocates it; its contents on entry do
+ * not matter (the call initialises what it reads).
  */
 size_t ra_bwd_workspace_size(int batch, int seq, int heads, int head_dim, ra_dtype dtype);
 
