@@ -161,15 +161,19 @@ def to_pinned(x, torch):
     return t.pin_memory()
 
 
-def time_fwd(ops, torch, w, steps, warmup, dev, keep_kv=False):
-    """Forward-only timing of workload w (device-resident inputs).  With keep_kv
-    the device K and V are returned too (the decode leg reads them as its cache)."""
+def time_fwd(ops, torch, w, steps, warmup, dev, keep_kv=False, with_seg=False):
+    """Forward-only timing of workload w (device-resident inputs, with the
+    workload's segment ids when it has them).  With keep_kv the device K and V are
+    returned too (the decode leg reads them as its cache); with with_seg the host
+    segment ids are returned too."""
     x = make_inputs(w, with_dout=False)
     q, k, v = (to_dev(getattr(x, n), torch, dev) for n in ("q", "k", "v"))
+    seg_h = x.segment_ids
+    seg = torch.from_numpy(np.ascontiguousarray(seg_h)).to(dev) if seg_h is not None else None
     del x
     out = torch.empty_like(q)
     lse = torch.empty((w.batch, w.heads, w.seq), dtype=torch.float32, device=dev)
-    args = (None, w.causal_block_size, w.num_shards, w.query_chunk_size, w.key_chunk_size)
+    args = (seg, w.causal_block_size, w.num_shards, w.query_chunk_size, w.key_chunk_size)
     for _ in range(warmup):
         ops.fwd(q, k, v, *args, out=out, lse=lse)
     ops.sync_check()
@@ -186,6 +190,8 @@ def time_fwd(ops, torch, w, steps, warmup, dev, keep_kv=False):
     fl = F.fwd_flops_nominal(w.batch, w.seq, w.heads, w.head_dim, w.causal_block_size > 0)
     if keep_kv:
         return fl, ms, (k, v)
+    if with_seg:
+        return fl, ms, seg_h
     return fl, ms
 
 
@@ -407,6 +413,28 @@ def gpu_arm(args, peaks, peaks_src):
                          "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_source": peaks_src,
                          "algorithmic_bytes": dbytes,
                          "traffic": profile_traffic("decode128_7b", dec_sha)}}
+        # the other forward evaluation workloads: causal B2 S8192 (config 2) and packed documents (config 3)
+        for cfg in (2, 3):
+            if cfg == args.workload:
+                continue
+            wc = WORKLOADS[cfg]
+            flc, msc, segc = time_fwd(ops, torch, wc, max(10, args.steps), max(3, args.warmup), dev, with_seg=True)
+            msm = statistics.mean(msc)
+            tfc = flc / (msm * 1e-3) / 1e12
+            line = {"workload": wc.name, "ms": round(msm, 4), "ms_min": round(min(msc), 4),
+                    "roofline": {"bound": "tensor", "kernel": f"fwd_bf16_kernel<{wc.head_dim}>",
+                                 "achieved": round(tfc, 1), "peak": peak, "unit": UNIT,
+                                 "frac": round(tfc / peak, 4), "frac_sustained": round(tfc / peak_s, 4),
+                                 "peak_source": peaks_src, "flops_per_launch": flc,
+                                 "traffic": profile_traffic(f"fwd{wc.head_dim}_cfg{cfg}", fwd_sha)}}
+            if segc is not None:  # packed documents: the visible pairs are the honest work
+                flv = F.fwd_flops_visible(wc.batch, wc.seq, wc.heads, wc.head_dim, wc.causal_block_size, segc)
+                tfv = flv / (msm * 1e-3) / 1e12
+                line["roofline"].update({"visible_flops_per_launch": flv, "achieved_visible": round(tfv, 1),
+                                         "frac_visible": round(tfv / peak, 4), "frac": round(tfv / peak, 4),
+                                         "achieved": round(tfv, 1), "achieved_nominal": round(tfc, 1),
+                                         "note": "achieved and frac count visible pairs only"})
+            extra[f"fwd_cfg{cfg}"] = line
         # blockwise feed-forward at the 7B shape (the other half of a blockwise transformer layer)
         wf = FFN_WORKLOADS["7b"]
         fms, ffl = time_ffn(ops, torch, wf, max(5, args.steps), max(3, args.warmup), dev)
@@ -601,12 +629,55 @@ def oracle_rows_rate(w, budget_s, x=None, start_rows=32):
     return total_f / total_t / 1e12, total_rows, total_t, oracle_threads()[0]
 
 
+def oracle_bwd_rate(w, budget_s, x=None, prefix=8192):
+    """Time the float64 backward oracle (ref_bwd_head_blocked) on whole heads of a
+    prefix of workload w: the first `prefix` positions of a drawn (b, h) head are
+    a complete attention problem of their own under the causal mask (no query of
+    the prefix sees a later key).  Returns (algorithmic TFLOP/s of the backward
+    under the metric's convention, heads, seconds)."""
+    import oracle
+
+    from long_context_exact_ra_gb300.inputs import bf16_bits_to_f32
+    if x is None:
+        x = make_inputs(w, with_dout=True)
+    n = min(prefix, w.seq) if w.causal_block_size > 0 else w.seq
+    g = np.random.Generator(np.random.PCG64(8))
+    rows = np.arange(n)
+    total_t, total_f, heads = 0.0, 0.0, 0
+    while total_t < budget_s or heads == 0:
+        b, h = int(g.integers(w.batch)), int(g.integers(w.heads))
+        Q, K, V, dO = (bf16_bits_to_f32(getattr(x, a)[b, :n, h]).astype(np.float64) for a in ("q", "k", "v", "dout"))
+        seg = None if x.segment_ids is None else x.segment_ids[b, :n]
+        t0 = time.perf_counter()
+        oracle.ref_bwd_head_blocked(Q, K, V, dO, seg, w.causal_block_size, rows, rows, block=2048)
+        total_t += time.perf_counter() - t0
+        total_f += F.bwd_flops_nominal(1, n, 1, w.head_dim, w.causal_block_size > 0)
+        heads += 1
+    return total_f / total_t / 1e12, heads, total_t, n
+
+
+def oracle_step_rate(w, budget_s, x=None):
+    """CPU oracle rate for one step of workload w: the forward on sampled query rows
+    and, for a forward+backward workload, the backward on whole prefix heads; the
+    step's FLOPs divided by the time the two rates imply for them."""
+    tf_f, rows, secs_f, cores = oracle_rows_rate(w, budget_s / (2 if w.backward else 1), x)
+    fl_f = F.fwd_flops_nominal(w.batch, w.seq, w.heads, w.head_dim, w.causal_block_size > 0)
+    if not w.backward:
+        return tf_f, cores, (f"float64 oracle forward on {rows} sampled query rows of '{w.name}' "
+                             f"(full key range per row, {secs_f:.1f} s); algorithmic FLOPs of the visible pairs")
+    tf_b, heads, secs_b, n = oracle_bwd_rate(w, budget_s / 2, x)
+    fl_b = F.bwd_flops_nominal(w.batch, w.seq, w.heads, w.head_dim, w.causal_block_size > 0)
+    value = (fl_f + fl_b) / (fl_f / (tf_f * 1e12) + fl_b / (tf_b * 1e12)) / 1e12
+    return value, cores, (f"float64 oracle: forward on {rows} sampled query rows of '{w.name}' ({secs_f:.1f} s, "
+                          f"{tf_f:.4f} TFLOP/s) and backward on {heads} whole heads of its first {n} positions "
+                          f"({secs_b:.1f} s, {tf_b:.4f} TFLOP/s); combined over the step's forward and backward "
+                          f"FLOPs (bwd = 2.5x fwd)")
+
+
 def cpu_baseline(w, budget_s=15.0):
-    tf, rows, secs, cores = oracle_rows_rate(w, budget_s)
-    return {"value": tf, "unit": UNIT, "cores": cores, "blas_threads": oracle_threads()[1], "kind": "oracle",
-            "sample": f"float64 oracle forward on {rows} sampled query rows of '{w.name}' "
-                      f"(full key range per row, {secs:.1f} s); algorithmic FLOPs of the visible pairs; "
-                      f"the backward is not sampled (same FLOP convention applies)"}
+    value, cores, sample = oracle_step_rate(w, budget_s)
+    return {"value": value, "unit": UNIT, "cores": cores, "blas_threads": oracle_threads()[1], "kind": "oracle",
+            "sample": sample}
 
 
 def cpu_baseline_decode(wd, budget_s=5.0, cache_len=16384):
@@ -664,15 +735,16 @@ def reference_arm(args):
     if rank != 0:
         return
     w = workload_for(args)
-    x = make_inputs(w, with_dout=False)
-    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    x = make_inputs(w, with_dout=w.backward)
+    per_step = max(4.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        oracle_rows_rate(w, per_step, x)
+        oracle_step_rate(w, per_step, x)
     rates, secs = [], 0.0
     for _ in range(args.steps):
-        tf, rows, s, cores = oracle_rows_rate(w, per_step, x)
+        t0 = time.perf_counter()
+        tf, cores, sample = oracle_step_rate(w, per_step, x)
+        secs += time.perf_counter() - t0
         rates.append(tf)
-        secs += s
     value = statistics.mean(rates)
     res = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
@@ -682,8 +754,7 @@ def reference_arm(args):
                       "head_dim": w.head_dim, "num_shards": w.num_shards},
            "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": cores,
                             "blas_threads": oracle_threads()[1],
-                            "sample": f"each step: float64 oracle forward on sampled query rows for "
-                                      f"~{per_step:.0f} s"},
+                            "sample": f"each step (~{per_step:.0f} s): {sample}"},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 

@@ -212,6 +212,118 @@ uint64_t ra_kernel_launches(void);
 ra_status ra_selftest_timeout(int64_t limit_ns, void* stream);
 
 /*
+ * Debug: record the tiles the tensor-core attention kernels visit, so that the
+ * ring order can be checked (the result alone cannot show it: it does not
+ * depend on the visit order beyond rounding, paper review page, 排列不变性).
+ *   buf : device memory of n int32 words, 16-byte aligned, or NULL to stop
+ *         recording.  n >= 16.
+ * From this call on, every bf16 ra_fwd, ra_bwd, ra_bwd_noalloc and ring-step
+ * call made by the calling thread (until the next ra_debug_visitlog) has its
+ * kernels append one entry per visited tile:
+ *   buf[0]          entries claimed so far (atomically incremented; it keeps
+ *                   counting past the capacity, so an overflow shows).  The
+ *                   caller zeroes it before the calls it wants recorded.
+ *   buf[1..7]       reserved.
+ *   entry e (e < (n - 8) / 8) at buf[8 + 8e .. 8 + 8e + 7]:
+ *     [0] kind (0 = forward, 1 = backward) | CTA index << 8
+ *     [1] batch index, [2] head
+ *     [3] the unit's home shard: the query shard j (forward) or key shard k
+ *         (backward) of the unit of work
+ *     [4] the unit's tile in that shard: query tile pair (forward: query tiles
+ *         2u and 2u+1 of 128 rows) or key tile of 128 rows (backward)
+ *     [5] ring step i
+ *     [6] visited shard: the key shard (forward, k = (j - i) mod N) or query
+ *         shard (backward, (k + i) mod N; paper review page, 环形注意力算法)
+ *     [7] visited tile of 128 rows within that shard
+ * One unit's entries are claimed in the order it visits its tiles.  Ring-step
+ * calls record with shard 0 (each is one block).  Recording costs an atomic
+ * per tile; with buf = NULL (the default) the kernels skip it.  The fp32 path
+ * records nothing.
+ */
+ra_status ra_debug_visitlog(int32_t* buf, size_t n);
+
+/*
+ * Ring steps across devices (context parallelism; paper review page, 环形通信
+ * and 环形注意力算法; code walk-through page, 环形计算模式).  Each device
+ * holds one block of `block_len` positions of the sequence: its query block and,
+ * at ring step i, the key/value block that has travelled i hops around the
+ * ring.  These calls do the device-local work of one step; moving blocks
+ * between devices is the caller's (a host ring driver over send/receive).
+ *
+ * Positions: query i of the block sits at global position q_pos0 + i * pos_stride
+ * and key t at k_pos0 + t * pos_stride.  Contiguous blocks (device r holds
+ * positions r * block_len ...) use pos_stride 1; striped blocks (device r
+ * holds r, r + N, r + 2N, ...) use pos_stride N (paper review page, 相关工作:
+ * Striped Attention, which spreads causal work evenly over the ring).  The
+ * masks are the forward's, on global positions: causal_block_size c > 0 makes
+ * key t visible to query i iff pos_q / c >= pos_k / c; with pos_stride > 1 only
+ * c in {0, 1} is supported (RA_ERR_UNSUPPORTED otherwise).  Segment ids come
+ * per block: q_segment_ids for the query block and kv_segment_ids for the
+ * key/value block ([batch, block_len] int32 each; both or neither).
+ * Requirements: as ra_fwd with seq = block_len and one shard, dtype RA_BF16,
+ * head_dim 64 or 128, q_pos0, k_pos0 >= 0 and every position < 2^30.
+ * Each call is asynchronous on `stream`; the carries are caller-owned device
+ * memory that the call reads and updates.
+ *
+ * ra_ring_fwd_step: merges attention(q block, k/v block) into the running
+ * carry: o_carry [batch, block_len, heads, head_dim] float32, the output so far
+ * (normalised), and lse_carry [batch, heads, block_len] float32, its natural-log
+ * log-sum-exp (-inf = nothing seen yet; start from o = 0, lse = -inf).  The
+ * merge is the lazy-softmax update (code walk-through page §2) at block
+ * granularity: with l_old, l_blk the two log-sum-exps, the new lse is
+ * log(e^l_old + e^l_blk) and the new output the e^l-weighted mean of the old
+ * carry and this block's output.  Rows with no visible key in the block keep
+ * their carry.  After the last step, ra_ring_finish turns o_carry into the bf16
+ * output; lse_carry is the output's lse.
+ */
+ra_status ra_ring_fwd_step(const void* q, const void* k, const void* v,
+                           const int32_t* q_segment_ids, const int32_t* kv_segment_ids,
+                           int causal_block_size, long long q_pos0, long long k_pos0, int pos_stride,
+                           int batch, int block_len, int heads, int head_dim, ra_dtype dtype,
+                           float* o_carry, float* lse_carry, void* stream);
+
+/*
+ * Backward ring steps.  The gradients of the query block accumulate on its
+ * device; the gradients of a key/value block travel around the ring with it
+ * (dK, dV float32 carries, [batch, block_len, heads, head_dim], start at 0):
+ *   ra_ring_bwd_begin : once per device, before the steps: from this device's
+ *                       final out (bf16), lse (the forward's lse_carry) and dout,
+ *                       stores Delta = rowsum(dout * out) and lse in the
+ *                       workspace and zeroes its dQ accumulator.
+ *   ra_ring_bwd_step  : per ring step: adds dQ of (query block, k/v block) to
+ *                       the workspace accumulator and dK, dV of the pair to
+ *                       dk_carry, dv_carry (P recomputed from lse, as ra_bwd).
+ *   ra_ring_bwd_end   : once, after the steps: dq (bf16) from the accumulator.
+ * The workspace holds ra_ring_bwd_workspace_size(...) bytes (16-byte aligned)
+ * and must not be shared by two devices' blocks.  When a key/value block is back
+ * on its home device after the last step, ra_ring_finish turns its carries into
+ * the bf16 dk and dv.
+ */
+size_t ra_ring_bwd_workspace_size(int batch, int block_len, int heads, int head_dim, ra_dtype dtype);
+
+ra_status ra_ring_bwd_begin(const void* out, const float* lse, const void* dout,
+                            int batch, int block_len, int heads, int head_dim, ra_dtype dtype,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+ra_status ra_ring_bwd_step(const void* q, const void* k, const void* v, const void* dout,
+                           const int32_t* q_segment_ids, const int32_t* kv_segment_ids,
+                           int causal_block_size, long long q_pos0, long long k_pos0, int pos_stride,
+                           int batch, int block_len, int heads, int head_dim, ra_dtype dtype,
+                           float* dk_carry, float* dv_carry,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+ra_status ra_ring_bwd_end(void* workspace, size_t workspace_bytes,
+                          int batch, int block_len, int heads, int head_dim, ra_dtype dtype,
+                          void* dq, void* stream);
+
+/*
+ * dst[i] = bf16(src[i]) (round to nearest even) for i < count: the last step of
+ * a ring, from a float32 carry to the bf16 result.  dtype must be RA_BF16;
+ * count a multiple of 4; both pointers 16-byte aligned.  One launch on `stream`.
+ */
+ra_status ra_ring_finish(const float* src, void* dst, size_t count, ra_dtype dtype, void* stream);
+
+/*
  * Size in bytes of the built-in scratch array used by ra_bwd_noalloc (64 MiB).
  * The pages have no counterpart to this entry point; it exists for callers
  * that cannot allocate device memory.
@@ -228,9 +340,14 @@ ra_status ra_selftest_timeout(int64_t limit_ns, void* stream);
  * no cudaMalloc, cudaFree or other allocating routine.
  *   - Problems whose ra_bwd_workspace_size(...) exceeds the array are
  *     rejected with RA_ERR_INVALID_ARG (use ra_bwd instead).
- *   - The first call on a device looks up the array's device address (once,
- *     with that device current); make that first call before any stream
- *     capture.
+ *   - Every call looks up the array's device address with the calling
+ *     thread's current device (so a device reset leaves no stale address).
+ *     The first call on a device is special: it loads the array onto that
+ *     device (64 MiB of device memory, which can fail with an out-of-memory
+ *     error or synchronize the device) and, like the first call of any entry
+ *     point here, clears the library's device status word with a blocking
+ *     memset.  Make that first call at start-up, while allocating and
+ *     synchronizing are still allowed, and before any stream capture.
  *   - All calls on a device share the array, which keeps the last call's
  *     contents (the part that must start at zero is cleared by every call).
  *     Calls that overlap on the GPU (unordered streams) race on it.

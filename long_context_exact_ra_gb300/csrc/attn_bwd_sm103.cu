@@ -27,8 +27,10 @@
 //   3. finalize: dq = bf16(dQ_accum / sqrt(d)).
 // Tensor memory (512 columns): A | B | dK | dV with A = S^T, later P^T, later
 // dQ_tile; B = dP^T, later dS^T.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cudaTypedefs.h>
 
 #include "ra_internal.h"
@@ -114,6 +116,17 @@ struct BwdParams {
   float scale_log2;  // log2(e) / sqrt(D)
   int* unit_counter; // zeroed by the preprocess kernel: CTAs draw tickets as they free up
   int group_heads;   // (b, h) heads per ticket group (their Q, dO, dQ accumulator fit in part of L2)
+  // Positions and key segment ids: query row r sits at position r + qoff, key row
+  // x at x + koff (0 and 0 for one sequence cut into virtual shards); kseg holds
+  // the key rows' segment ids (p.seg for one sequence).
+  int qoff, koff;
+  const int32_t* kseg;
+  // Ring-step carries (kCarry kernels only): fp32 dK, dV [B, S, H, D] that this
+  // call's key-block gradients are added to.
+  float* dk_carry;
+  float* dv_carry;
+  int* vlog;     // visit log (see visit_log), or null
+  int vlog_cap;
 };
 
 __device__ __forceinline__ void red_add_v2(float* addr, float a, float b) {
@@ -207,7 +220,7 @@ __device__ __forceinline__ int bticket_unit(const BwdParams& P, int t) {
 // ---------------------------------------------------------------------------
 // 2. main kernel
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool kCarry>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
@@ -268,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int rec_n = 0, pair_n = 0, unit_n = 0, kv_loads = 0;
     bool alive = true;
     const int c = pb.causal;
+    const int qo = kCarry ? P.qoff : 0, ko = kCarry ? P.koff : 0;
     auto publish = [&](const BRec& r) -> bool {
       const int slot = rec_n % kNInfo;
       if (!mbar_wait(bars.infoempty(slot), ((rec_n / kNInfo) & 1) ^ 1, ctl, 40)) return false;
@@ -299,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pb.seg) {
         int mn = INT_MAX, mx = INT_MIN;
         for (int r = lane; r < kvalid; r += 32) {
-          const int sv = __ldg(pb.seg + (size_t)b * pb.S + k0 + r);
+          const int sv = __ldg((kCarry ? P.kseg : pb.seg) + (size_t)b * pb.S + k0 + r);
           mn = min(mn, sv);
           mx = max(mx, sv);
         }
@@ -325,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < pb.N && alive; ++i) {
         const int js = (k + i) % pb.N;  // the ring device holding this key block at step i
         const int qbeg = js * pb.Ssh, qend = qbeg + pb.Ssh;
-        if (c > 0 && (qend - 1) / c < k0 / c) continue;  // every query of the shard precedes the keys
+        if (c > 0 && (qend - 1 + qo) / c < (k0 + ko) / c) continue;  // every query of the shard precedes the keys
         for (int t0 = 0; t0 < P.tiles_per_shard && alive; t0 += 32) {
           int qmn = 0, qmx = 0;
           const int my_t = t0 + lane;
@@ -333,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qa = qbeg + my_t * kT;
             const int qb = min(qend, qa + kT);
             int mn = INT_MAX, mx = INT_MIN;
-            if (!(c > 0 && (qb - 1) / c < k0 / c)) {
+            if (!(c > 0 && (qb - 1 + qo) / c < (k0 + ko) / c)) {
               const int* sp = pb.seg + (size_t)b * pb.S;
               for (int x = qa; x < qb; ++x) {
                 const int sv = __ldg(sp + x);
@@ -353,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tmx = __shfl_sync(0xffffffffu, qmx, tt);
             bool skip = false, full = true;
             if (c > 0) {
-              if (ql / c < k0 / c) skip = true;
-              else if (!(qa / c >= klast / c)) full = false;
+              if ((ql + qo) / c < (k0 + ko) / c) skip = true;
+              else if (!((qa + qo) / c >= (klast + ko) / c)) full = false;
             }
             if (!skip && pb.seg) {
               if (tmx < kmn || tmn > kmx) skip = true;
@@ -386,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               r.k0 = k0;
               r.kvalid = kvalid;
               alive = publish(r);
+              if (P.vlog) visit_log(P.vlog, P.vlog_cap, 1, b, h, k, t, i, js, t0 + tt);
             }
             alive = __shfl_sync(0xffffffffu, alive, 0);
             ++pair_n;
@@ -562,10 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         sp_ph ^= 1;
         tc_fence_after();
         const bool masked = r.flags & kMasked;
-        const int kpos = r.k0 + kr;
+        const int kidx = r.k0 + kr;
         const int cb = pb.causal;
-        const int kblk = cb > 0 ? kpos / cb : 0;
-        const int kseg = (pb.seg && kr < r.kvalid) ? __ldg(pb.seg + (size_t)r.b * pb.S + kpos) : 0;
+        const int kblk = cb > 0 ? (kidx + (kCarry ? P.koff : 0)) / cb : 0;
+        const int kseg = (pb.seg && kr < r.kvalid) ? __ldg((kCarry ? P.kseg : pb.seg) + (size_t)r.b * pb.S + kidx) : 0;
         // this warpgroup's 64 query columns in quarters of 16: S^T from A, dP^T from B;
         // each quarter's 16 B columns become 8 columns of dS^T then 8 of P^T (bf16 pairs)
         uint32_t sv[16], dp[16];
@@ -592,10 +607,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int y = 0; y < 16; ++y) {
               const int cc = c0 + y;
-              const int qpos = r.q0 + cc;
+              const int qidx = r.q0 + cc;
               bool vis = (kr < r.kvalid) & (cc < r.qvalid);
-              vis &= (cb <= 0) | (qpos / max(cb, 1) >= kblk);
-              const int qs = qsegp ? __ldg(qsegp + min(qpos, pb.S - 1)) : kseg;
+              vis &= (cb <= 0) | ((qidx + (kCarry ? P.qoff : 0)) / max(cb, 1) >= kblk);
+              const int qs = qsegp ? __ldg(qsegp + min(qidx, pb.S - 1)) : kseg;
               vis &= (qs == kseg);
               pq[y] = vis ? pq[y] : 0.f;
             }
@@ -686,26 +701,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t tacc = tbase + (wg == 0 ? C::TDK : C::TDV) + lane_off;
         const float mul = wg == 0 ? P.scale : 1.f;
-        __nv_bfloat16* dst = (wg == 0 ? P.dk : P.dv) + (((size_t)r.b * pb.S + r.k0 + kr) * pb.H + r.h) * D;
+        const size_t row = ((size_t)r.b * pb.S + r.k0 + kr) * pb.H + r.h;
 #pragma unroll
         for (int cq = 0; cq < D / 32; ++cq) {
           uint32_t o[32];
           tmem_ld32(tacc + cq * 32, o);
           tmem_ld_wait(o);
-          if (unit_pairs == 0) {  // no visible query: the gradient is zero
+          if constexpr (!kCarry) {
+            __nv_bfloat16* dst = (wg == 0 ? P.dk : P.dv) + row * D;
+            if (unit_pairs == 0) {  // no visible query: the gradient is zero
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] = 0u;
-          }
-          if (kr < r.kvalid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + cq * 32);
+              for (int x = 0; x < 32; ++x) o[x] = 0u;
+            }
+            if (kr < r.kvalid) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + cq * 32);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint4 val;
-              val.x = pack_bf16x2(__uint_as_float(o[v4 * 8 + 0]) * mul, __uint_as_float(o[v4 * 8 + 1]) * mul);
-              val.y = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2]) * mul, __uint_as_float(o[v4 * 8 + 3]) * mul);
-              val.z = pack_bf16x2(__uint_as_float(o[v4 * 8 + 4]) * mul, __uint_as_float(o[v4 * 8 + 5]) * mul);
-              val.w = pack_bf16x2(__uint_as_float(o[v4 * 8 + 6]) * mul, __uint_as_float(o[v4 * 8 + 7]) * mul);
-              d4[v4] = val;
+              for (int v4 = 0; v4 < 4; ++v4) {
+                uint4 val;
+                val.x = pack_bf16x2(__uint_as_float(o[v4 * 8 + 0]) * mul, __uint_as_float(o[v4 * 8 + 1]) * mul);
+                val.y = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2]) * mul, __uint_as_float(o[v4 * 8 + 3]) * mul);
+                val.z = pack_bf16x2(__uint_as_float(o[v4 * 8 + 4]) * mul, __uint_as_float(o[v4 * 8 + 5]) * mul);
+                val.w = pack_bf16x2(__uint_as_float(o[v4 * 8 + 6]) * mul, __uint_as_float(o[v4 * 8 + 7]) * mul);
+                d4[v4] = val;
+              }
+            }
+          } else {
+            // Ring step: this key block's gradients from this query block are added
+            // to the carries that travel around the ring with K and V.  Each unit
+            // owns its key rows, so the read-modify-write does not race.
+            if (unit_pairs > 0 && kr < r.kvalid) {
+              float4* d4 = reinterpret_cast<float4*>((wg == 0 ? P.dk_carry : P.dv_carry) + row * D + cq * 32);
+#pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4) {
+                float4 c4 = d4[v4];
+                c4.x += __uint_as_float(o[v4 * 4 + 0]) * mul;
+                c4.y += __uint_as_float(o[v4 * 4 + 1]) * mul;
+                c4.z += __uint_as_float(o[v4 * 4 + 2]) * mul;
+                c4.w += __uint_as_float(o[v4 * 4 + 3]) * mul;
+                d4[v4] = c4;
+              }
             }
           }
         }
@@ -726,8 +760,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D>
-static cudaError_t launch_bwd_bf16_d(const BwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
+// Stages of the backward (BwdArgs::stage): the whole backward on one sequence,
+// or one of the three parts a ring of separate blocks runs (begin once,
+// one step per key/value block, end once).
+template <int D, bool kCarry>
+static cudaError_t launch_bwd_main(const BwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
   using Cf = BCfg<D>;
   const Problem& p = a.p;
   CUtensorMap mq, mk, mv, mdo;
@@ -736,18 +773,10 @@ static cudaError_t launch_bwd_bf16_d(const BwdArgs& a, const Ctx& c, uint64_t* l
     *why = "cuTensorMapEncodeTiled failed (driver entry point unavailable or tensor rejected)";
     return cudaSuccess;
   }
-  const long long rows = (long long)p.B * p.S * p.H;
-  const int Sp = bwd_row_pitch(p.S);
-  bwd_pre_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, c.stream>>>(
-      p, (const __nv_bfloat16*)a.out, (const __nv_bfloat16*)a.dout, a.lse, (float2*)a.delta, Sp, a.dq_accum,
-      a.unit_counter);
-  *launches += 1;
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   BwdParams P;
   P.p = p;
   P.ld2 = (const float2*)a.delta;
-  P.Sp = Sp;
+  P.Sp = bwd_row_pitch(p.S);
   P.dq_accum = a.dq_accum;
   P.dk = (__nv_bfloat16*)a.dk;
   P.dv = (__nv_bfloat16*)a.dv;
@@ -758,23 +787,64 @@ static cudaError_t launch_bwd_bf16_d(const BwdArgs& a, const Ctx& c, uint64_t* l
   P.scale = (float)(1.0 / sqrt((double)p.D));
   P.scale_log2 = (float)(1.4426950408889634 / sqrt((double)p.D));
   P.unit_counter = a.unit_counter;
+  P.qoff = a.qoff;
+  P.koff = a.koff;
+  P.kseg = a.kseg ? a.kseg : p.seg;
+  P.dk_carry = a.dk_carry;
+  P.dv_carry = a.dv_carry;
+  P.vlog = a.vlog;
+  P.vlog_cap = a.vlog_cap;
   {  // heads whose Q, dO (bf16) and dQ accumulator (fp32), 8 * S * D bytes, fit in 48 MB of L2
     const long long per = 8LL * p.S * p.D;
     P.group_heads = (int)std::max(1LL, std::min((long long)p.B * p.H, (48LL << 20) / per));
   }
-  static bool attr_set[256][2];
-  const int di = D == 64 ? 0 : 1;
-  if (!attr_set[c.device][di]) {
-    e = cudaFuncSetAttribute(bwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM);
+  static std::atomic<bool> attr_set[256][2];  // idempotent attribute; atomic so threads may race
+  if (!attr_set[c.device][kCarry]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_bf16_kernel<D, kCarry>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set[c.device][di] = true;
+    attr_set[c.device][kCarry] = true;
   }
   const int grid = std::min(c.num_sms, P.num_units);
-  bwd_bf16_kernel<D><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, mdo, P);
+  bwd_bf16_kernel<D, kCarry><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, mdo, P);
   *launches += 1;
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t n4 = (size_t)rows * p.D / 4;
-  bwd_fin_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(n4, (const float4*)a.dq_accum, (uint2*)a.dq, P.scale);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_bwd_bf16_d(const BwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
+  const Problem& p = a.p;
+  const long long rows = (long long)p.B * p.S * p.H;
+  cudaError_t e;
+  if (a.stage == kBwdWhole || a.stage == kBwdRingBegin) {
+    bwd_pre_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, c.stream>>>(
+        p, (const __nv_bfloat16*)a.out, (const __nv_bfloat16*)a.dout, a.lse, (float2*)a.delta, bwd_row_pitch(p.S),
+        a.dq_accum, a.unit_counter);
+    *launches += 1;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (a.stage == kBwdWhole) {
+    e = launch_bwd_main<D, false>(a, c, launches, why);
+    if (e != cudaSuccess || *why) return e;
+  } else if (a.stage == kBwdRingStep) {
+    // every launch of the main kernel starts from a zero unit counter
+    if ((e = cudaMemsetAsync(a.unit_counter, 0, sizeof(int), c.stream)) != cudaSuccess) return e;
+    e = launch_bwd_main<D, true>(a, c, launches, why);
+    if (e != cudaSuccess || *why) return e;
+  }
+  if (a.stage == kBwdWhole || a.stage == kBwdRingEnd) {
+    const size_t n4 = (size_t)rows * p.D / 4;
+    bwd_fin_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(n4, (const float4*)a.dq_accum, (uint2*)a.dq,
+                                                        (float)(1.0 / sqrt((double)p.D)));
+    *launches += 1;
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_cast_bf16(const float* src, void* dst, size_t count, float scale, const Ctx& c,
+                             uint64_t* launches) {
+  bwd_fin_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(count / 4, (const float4*)src, (uint2*)dst, scale);
   *launches += 1;
   return cudaGetLastError();
 }

@@ -28,6 +28,7 @@
 // exceeds it by more than 2^8; in exact arithmetic the result is unchanged
 // (numerator and denominator carry the same factor), and the exponentials
 // stay <= 256.  Every mbarrier wait is bounded (see sm103.cuh).
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -101,6 +102,18 @@ struct FwdParams {
   Problem p;
   __nv_bfloat16* out;
   float* lse;
+  // Positions and key segment ids.  Query row r sits at position r + qoff and key
+  // row x at x + koff (both 0 for one sequence cut into virtual shards; a ring
+  // step between two separate blocks passes their global offsets).  kseg holds the
+  // key rows' segment ids (the same array as p.seg for one sequence).
+  int qoff, koff;
+  const int32_t* kseg;
+  // Ring-step carry (kCarry kernels only): fp32 running output [B, S, H, D] and
+  // natural-log lse [B, H, S] that this call's result is merged into.
+  float* o_carry;
+  float* lse_carry;
+  int* vlog;            // visit log (see visit_log), or null
+  int vlog_cap;         // entries the log holds
   int* status;
   uint64_t limit_ns;
   int tiles_per_shard;  // ceil(Ssh / 128)
@@ -143,7 +156,7 @@ __device__ __forceinline__ int ticket_unit(const FwdParams& P, int t) {
   return (g0 + (w - rank * gh)) * per_head + rank;
 }
 
-template <int D>
+template <int D, bool kCarry>
 __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-partitions -> <= 168 registers
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const FwdParams P) {
@@ -203,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
     int rec_n = 0, tile_n = 0, unit_n = 0, q_loads = 0;
     bool alive = true;
     const int c = pb.causal;
+    const int qo = kCarry ? P.qoff : 0, ko = kCarry ? P.koff : 0;
     // publish a record (lane 0 only); returns false on abort
     auto publish = [&](const Rec& r) -> bool {
       const int slot = rec_n % kNInfo;
@@ -292,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
       for (int i = 0; i < pb.N && alive; ++i) {
         const int ks = ((j - i) % pb.N + pb.N) % pb.N;  // ring order
         const int kbeg = ks * pb.Ssh, kend = kbeg + pb.Ssh;
-        if (c > 0 && floordiv_pos(qlast, c) < floordiv_pos(kbeg, c)) continue;  // whole shard in the future
+        if (c > 0 && floordiv_pos(qlast + qo, c) < floordiv_pos(kbeg + ko, c)) continue;  // whole shard in the future
         for (int t0 = 0; t0 < P.tiles_per_shard && alive; t0 += 32) {
           // tile segment ranges, one tile per lane
           int kmn = 0, kmx = 0;
@@ -300,10 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
           if (pb.seg && my_t < P.tiles_per_shard) {
             const int ka = kbeg + my_t * kBN;
             const int kb = min(kend, ka + kBN);
-            bool needed = !(c > 0 && floordiv_pos(qlast, c) < floordiv_pos(ka, c));
+            bool needed = !(c > 0 && floordiv_pos(qlast + qo, c) < floordiv_pos(ka + ko, c));
             int mn = INT_MAX, mx = INT_MIN;
             if (needed) {
-              const int* sp = pb.seg + (size_t)b * pb.S + ka;
+              const int* sp = (kCarry ? P.kseg : pb.seg) + (size_t)b * pb.S + ka;
               if (kb - ka == kBN && ((reinterpret_cast<uintptr_t>(sp) & 15u) == 0)) {
 #pragma unroll 8
                 for (int x4 = 0; x4 < kBN / 4; ++x4) {
@@ -335,8 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
               const int qa = q0 + w * kBM, ql = qa + qv - 1;
               bool skip = qv == 0, full = true;
               if (!skip && c > 0) {
-                if (floordiv_pos(ql, c) < floordiv_pos(ka, c)) skip = true;
-                else if (!(floordiv_pos(qa, c) >= floordiv_pos(kb, c))) full = false;
+                if (floordiv_pos(ql + qo, c) < floordiv_pos(ka + ko, c)) skip = true;
+                else if (!(floordiv_pos(qa + qo, c) >= floordiv_pos(kb + ko, c))) full = false;
               }
               if (!skip && pb.seg) {
                 if (kmx < qmin[w] || kmn > qmax[w]) skip = true;
@@ -372,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
               r.qvalid1 = qv1;
               if constexpr (D == 64) r.kseg = kseg;
               alive = publish(r);
+              if (P.vlog) visit_log(P.vlog, P.vlog_cap, 0, b, h, j, pr, i, ks, t0 + tt);
               const int s = tile_n % C::KST;
               const uint32_t par = ((tile_n / C::KST) & 1) ^ 1;
               if (alive) alive = mbar_wait(bars.kempty(s), par, ctl, 12);
@@ -600,7 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
           // keys x < nvis of the tile pass the range and causal rules: the causal
           // block of key kstart + x must not exceed the row's block
           long long lim = r.kvalid;
-          if (pb.causal > 0) lim = min(lim, ((long long)qrow / pb.causal + 1) * pb.causal - r.kstart);
+          if (pb.causal > 0)
+            lim = min(lim, ((long long)(qrow + (kCarry ? P.qoff : 0)) / pb.causal + 1) * pb.causal - (r.kstart + (kCarry ? P.koff : 0)));
           int nvis = (int)max(lim, 0LL);
           // With one segment id across the tile's keys (packed documents: the causal
           // diagonal tiles), a row sees all of the tile or none of it, and the 128 key
@@ -612,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
             if (__ldg(pb.seg + (size_t)r.b * pb.S + min(qrow, pb.S - 1)) != r.kseg) nvis = 0;
           }
           if (pb.seg && !uni) {
-            const int* ks = pb.seg + (size_t)r.b * pb.S + r.kstart;
+            const int* ks = (kCarry ? P.kseg : pb.seg) + (size_t)r.b * pb.S + r.kstart;
             const int qseg = __ldg(pb.seg + (size_t)r.b * pb.S + min(qrow, pb.S - 1));
             if (r.kvalid == 128 && ((reinterpret_cast<uintptr_t>(ks) & 15u) == 0)) {
               // the tile's 128 key ids in 16-byte loads (the same addresses for every row: L1 broadcast)
@@ -700,29 +716,71 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
           tc_fence_after();
           const int qv = w == 0 ? r.qvalid0 : r.qvalid1;
           const bool store = rl < qv;
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-          __nv_bfloat16* orow = P.out + (((size_t)r.b * pb.S + qrow) * pb.H + r.h) * D;
+          if constexpr (!kCarry) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16* orow = P.out + (((size_t)r.b * pb.S + qrow) * pb.H + r.h) * D;
 #pragma unroll
-          for (int cq = 0; cq < D / 32; ++cq) {
-            uint32_t o[32];
-            tmem_ld32(tO + cq * 32, o);
-            tmem_ld_wait(o);
-            if (store) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + cq * 32);
+            for (int cq = 0; cq < D / 32; ++cq) {
+              uint32_t o[32];
+              tmem_ld32(tO + cq * 32, o);
+              tmem_ld_wait(o);
+              if (store) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + cq * 32);
 #pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4) {
-                uint4 val;
-                val.x = pack_bf16x2(__uint_as_float(o[v4 * 8 + 0]) * inv, __uint_as_float(o[v4 * 8 + 1]) * inv);
-                val.y = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2]) * inv, __uint_as_float(o[v4 * 8 + 3]) * inv);
-                val.z = pack_bf16x2(__uint_as_float(o[v4 * 8 + 4]) * inv, __uint_as_float(o[v4 * 8 + 5]) * inv);
-                val.w = pack_bf16x2(__uint_as_float(o[v4 * 8 + 6]) * inv, __uint_as_float(o[v4 * 8 + 7]) * inv);
-                dst[v4] = val;
+                for (int v4 = 0; v4 < 4; ++v4) {
+                  uint4 val;
+                  val.x = pack_bf16x2(__uint_as_float(o[v4 * 8 + 0]) * inv, __uint_as_float(o[v4 * 8 + 1]) * inv);
+                  val.y = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2]) * inv, __uint_as_float(o[v4 * 8 + 3]) * inv);
+                  val.z = pack_bf16x2(__uint_as_float(o[v4 * 8 + 4]) * inv, __uint_as_float(o[v4 * 8 + 5]) * inv);
+                  val.w = pack_bf16x2(__uint_as_float(o[v4 * 8 + 6]) * inv, __uint_as_float(o[v4 * 8 + 7]) * inv);
+                  dst[v4] = val;
+                }
+              }
+            }
+            if (store)
+              P.lse[((size_t)r.b * pb.H + r.h) * pb.S + qrow] =
+                  l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          } else {
+            // Ring step: merge this block's (out, lse) into the running carry, the
+            // lazy-softmax update at block granularity (code walk-through page §2):
+            // with L the log2-sum-exp of the carry and of this block and M their
+            // max, carry = carry * 2^(L_old - M) / Z + out_blk * 2^(L_blk - M) / Z,
+            // Z = 2^(L_old - M) + 2^(L_blk - M), lse = (M + log2 Z) ln 2.  A row
+            // with no visible key in this block leaves its carry unchanged.
+            const bool merge = store && l > 0.f;
+            float wo = 0.f, wn = 0.f;
+            const size_t lidx = ((size_t)r.b * pb.H + r.h) * pb.S + qrow;
+            if (merge) {
+              const float L_blk = m_use + __log2f(l);
+              const float L_old = P.lse_carry[lidx] * 1.4426950408889634f;  // -inf stays -inf
+              const float M = fmaxf(L_old, L_blk);
+              const float a = ex2_approx(L_old - M);  // 0 for an empty carry
+              const float bb = ex2_approx(L_blk - M);
+              const float z = a + bb;
+              wo = a / z;
+              wn = bb / (z * l);
+              P.lse_carry[lidx] = (M + __log2f(z)) * 0.69314718055994531f;
+            }
+            float* oc = P.o_carry + (((size_t)r.b * pb.S + qrow) * pb.H + r.h) * D;
+#pragma unroll
+            for (int cq = 0; cq < D / 32; ++cq) {
+              uint32_t o[32];
+              tmem_ld32(tO + cq * 32, o);
+              tmem_ld_wait(o);
+              if (merge) {
+                float4* dst = reinterpret_cast<float4*>(oc + cq * 32);
+#pragma unroll
+                for (int v4 = 0; v4 < 8; ++v4) {
+                  float4 c4 = dst[v4];
+                  c4.x = c4.x * wo + __uint_as_float(o[v4 * 4 + 0]) * wn;
+                  c4.y = c4.y * wo + __uint_as_float(o[v4 * 4 + 1]) * wn;
+                  c4.z = c4.z * wo + __uint_as_float(o[v4 * 4 + 2]) * wn;
+                  c4.w = c4.w * wo + __uint_as_float(o[v4 * 4 + 3]) * wn;
+                  dst[v4] = c4;
+                }
               }
             }
           }
-          if (store)
-            P.lse[((size_t)r.b * pb.H + r.h) * pb.S + qrow] =
-                l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
           tc_fence_before();
           mbar_arrive(bars.ofree(w));
         }
@@ -816,7 +874,7 @@ static int* take_unit_counter(const Ctx& c) {
   return static_cast<int*>(p);
 }
 
-template <int D>
+template <int D, bool kCarry>
 static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
   using Cf = Cfg<D>;
   const Problem& p = a.p;
@@ -829,19 +887,25 @@ static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* l
   P.p = p;
   P.out = (__nv_bfloat16*)a.out;
   P.lse = a.lse;
+  P.qoff = a.qoff;
+  P.koff = a.koff;
+  P.kseg = a.kseg ? a.kseg : p.seg;
+  P.o_carry = a.o_carry;
+  P.lse_carry = a.lse_carry;
+  P.vlog = a.vlog;
+  P.vlog_cap = a.vlog_cap;
   P.status = c.status;
   P.limit_ns = c.limit_ns;
   P.tiles_per_shard = (p.Ssh + kBN - 1) / kBN;
   P.pairs_per_shard = (P.tiles_per_shard + 1) / 2;
   P.num_units = p.B * p.H * p.N * P.pairs_per_shard;
   P.scale_log2 = (float)(1.4426950408889634 / sqrt((double)p.D));
-  static bool attr_set[256][2];
-  const int di = D == 64 ? 0 : 1;
-  if (!attr_set[c.device][di]) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static std::atomic<bool> attr_set[256][2];  // idempotent attribute; atomic so threads may race
+  if (!attr_set[c.device][kCarry]) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, kCarry>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Cf::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set[c.device][di] = true;
+    attr_set[c.device][kCarry] = true;
   }
   const int per_head = p.N * P.pairs_per_shard;
   const int num_super = (P.num_units / per_head) * ((per_head + 1) / 2);  // balanced unit pairs
@@ -855,7 +919,7 @@ static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* l
     P.group_heads = (int)std::max(1LL, std::min((long long)p.B * p.H, (48LL << 20) / kv));
   }
   const int grid = std::min(c.num_sms, P.unit_counter ? P.num_units : num_super);
-  fwd_bf16_kernel<D><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, P);
+  fwd_bf16_kernel<D, kCarry><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, P);
   *launches += 1;
   cudaError_t e = cudaGetLastError();
   if (P.unit_counter) {
@@ -866,8 +930,11 @@ static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* l
 }
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
-  if (a.p.D == 64) return launch_fwd_bf16_d<64>(a, c, launches, why);
-  if (a.p.D == 128) return launch_fwd_bf16_d<128>(a, c, launches, why);
+  const bool carry = a.o_carry != nullptr;
+  if (a.p.D == 64) return carry ? launch_fwd_bf16_d<64, true>(a, c, launches, why)
+                                : launch_fwd_bf16_d<64, false>(a, c, launches, why);
+  if (a.p.D == 128) return carry ? launch_fwd_bf16_d<128, true>(a, c, launches, why)
+                                 : launch_fwd_bf16_d<128, false>(a, c, launches, why);
   *why = "bf16 head_dim must be 64 or 128";
   return cudaSuccess;
 }

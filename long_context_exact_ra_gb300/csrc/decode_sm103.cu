@@ -26,6 +26,7 @@
 //      memory into one partial (m, l, o) per CTA.
 //   2. combine kernel: one CTA per (batch, head, token) merges the partials in
 //      ring order and writes out = o / l and lse = (m + log2 l) * ln 2.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -488,7 +489,7 @@ __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(DecPara
 template <typename E, int D, int TM>
 cudaError_t launch_partial(const DecParams& p, dim3 grid, const Ctx& c) {
   constexpr int smem = dec_smem_bytes<E, D, TM>();
-  static bool attr_set[256];  // the attribute is per kernel and device, and idempotent
+  static std::atomic<bool> attr_set[256];  // the attribute is per kernel and device, and idempotent
   if (!attr_set[c.device]) {
     cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<E, D, TM>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

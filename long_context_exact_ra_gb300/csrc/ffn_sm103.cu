@@ -22,6 +22,7 @@
 // Every wait is bounded; on a timeout the kernel records the site in the
 // status word, drains its copies and MMAs, frees tensor memory and returns.
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -265,7 +266,7 @@ bool make_2d_map(CUtensorMap* m, const void* ptr, long long rows, long long cols
 
 cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, GemmParams P, const Ctx& c,
                         uint64_t* launches) {
-  static bool attr_set[256];
+  static std::atomic<bool> attr_set[256];  // idempotent attribute; atomic so threads may race
   if (!attr_set[c.device]) {
     cudaError_t e =
         cudaFuncSetAttribute(gemm_bias_act_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GCfg::SMEM);

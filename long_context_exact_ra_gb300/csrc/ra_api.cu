@@ -19,10 +19,11 @@ __device__ int g_status;  // kernels record a timed-out wait here (one word per 
 namespace {
 
 thread_local char t_msg[512] = "";
+thread_local int* t_vlog = nullptr;  // ra_debug_visitlog target of this thread
+thread_local int t_vlog_cap = 0;
 std::atomic<uint64_t> g_launches{0};
 std::mutex g_mu;
-int* g_status_ptr[256];
-bool g_status_init[256];
+int* g_status_ptr[256];  // last status-word address seen per device
 
 ra_status fail(ra_status s, const char* fmt, ...) {
   va_list ap;
@@ -52,18 +53,19 @@ ra_status make_ctx(void* stream, Ctx* c) {
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= 256) return fail(RA_ERR_CUDA, "device ordinal %d out of range", dev);
   {
+    // The status word's address is looked up on every call: after a device reset
+    // the module is loaded again, possibly elsewhere, and a cached address would
+    // be stale.  A word at an address not seen before is cleared once.
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status);
+    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_status_init[dev]) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_status);
-      if (e != cudaSuccess)
-        return fail(RA_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+    if (g_status_ptr[dev] != (int*)p) {
       e = cudaMemset(p, 0, sizeof(int));
       if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaMemset(status): %s", cudaGetErrorString(e));
       g_status_ptr[dev] = (int*)p;
-      g_status_init[dev] = true;
     }
-    c->status = g_status_ptr[dev];
+    c->status = (int*)p;
   }
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -115,6 +117,38 @@ ra_status validate(const void* const* ptrs, const char* const* names, int nptr,
   return RA_OK;
 }
 
+// Kernel position offsets for one ring step.  Query i of the block sits at
+// global position q_pos0 + i * stride and key t at k_pos0 + t * stride.  With
+// stride 1 the kernels compare global positions (offsets q_pos0, k_pos0).  With
+// stride > 1 (striped blocks) only causal_block_size 0 or 1 is defined here:
+// then key t is visible to query i iff t <= i + delta, delta =
+// floor((q_pos0 - k_pos0) / stride), which the kernels see as positions i + m
+// and t + m - delta with m = max(0, delta) (both offsets non-negative).
+ra_status ring_offsets(int c, long long q_pos0, long long k_pos0, int stride, int S, int* qoff, int* koff) {
+  if (q_pos0 < 0 || k_pos0 < 0 || stride < 1)
+    return fail(RA_ERR_INVALID_ARG, "positions must be >= 0 and pos_stride >= 1 (got %lld, %lld, %d)", q_pos0, k_pos0,
+                stride);
+  const long long span = (long long)(S > 0 ? S - 1 : 0) * stride;
+  if (q_pos0 + span >= (1LL << 30) || k_pos0 + span >= (1LL << 30))
+    return fail(RA_ERR_INVALID_ARG, "positions must stay below 2^30");
+  if (stride == 1) {
+    *qoff = (int)q_pos0;
+    *koff = (int)k_pos0;
+    return RA_OK;
+  }
+  if (c > 1) return fail(RA_ERR_UNSUPPORTED, "strided positions support causal_block_size 0 or 1, got %d", c);
+  if (c == 0) {
+    *qoff = *koff = 0;
+    return RA_OK;
+  }
+  const long long d = q_pos0 - k_pos0;
+  const long long delta = d >= 0 ? d / stride : -((-d + stride - 1) / stride);  // floor division
+  const long long m = delta > 0 ? delta : 0;
+  *qoff = (int)m;
+  *koff = (int)(m - delta);
+  return RA_OK;
+}
+
 }  // namespace
 
 // Record a message for ra_last_error() on behalf of entry points in other files.
@@ -142,6 +176,8 @@ RA_API ra_status ra_fwd(const void* q, const void* k, const void* v, const int32
   a.v = v;
   a.out = out;
   a.lse = lse;
+  a.vlog = t_vlog;
+  a.vlog_cap = t_vlog_cap;
   uint64_t n = 0;
   cudaError_t e;
   const char* why = nullptr;
@@ -190,6 +226,8 @@ RA_API ra_status ra_bwd(const void* q, const void* k, const void* v, const void*
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
+  a.vlog = t_vlog;
+  a.vlog_cap = t_vlog_cap;
   uint64_t n = 0;
   cudaError_t e;
   const char* why = nullptr;
@@ -388,5 +426,167 @@ RA_API ra_status ra_selftest_timeout(int64_t limit_ns, void* stream) {
   cudaError_t e = launch_selftest_timeout(c, &n);
   g_launches += n;
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "selftest launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+RA_API ra_status ra_debug_visitlog(int32_t* buf, size_t n) {
+  if (buf == nullptr) {
+    t_vlog = nullptr;
+    t_vlog_cap = 0;
+    return ok();
+  }
+  if (!aligned16(buf)) return fail(RA_ERR_INVALID_ARG, "visit log buffer is not 16-byte aligned");
+  if (n < 16) return fail(RA_ERR_INVALID_ARG, "visit log needs at least 16 words (8 header + one entry), got %zu", n);
+  const size_t cap = (n - 8) / 8;
+  t_vlog = buf;
+  t_vlog_cap = (int)(cap > 0x7fffffff ? 0x7fffffff : cap);
+  return ok();
+}
+
+// ----------------------------------------------------------------------------- ring steps
+
+namespace {
+
+ra_status ring_common(const void* const* ptrs, const char* const* names, int nptr, const int32_t* qseg,
+                      const int32_t* kseg, int c, long long q_pos0, long long k_pos0, int stride, int B, int S, int H,
+                      int D, ra_dtype dtype, Problem* p, CallExtras* x) {
+  if ((qseg == nullptr) != (kseg == nullptr))
+    return fail(RA_ERR_INVALID_ARG, "q_segment_ids and kv_segment_ids must be given together");
+  ra_status s = validate(ptrs, names, nptr, qseg, c, 1, S > 0 ? S : 1, S > 0 ? S : 1, B, S, H, D, dtype, p);
+  if (s != RA_OK) return s;
+  if (dtype != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "ring steps support bf16 only");
+  if (S > 0 && kseg != nullptr && !aligned16(kseg)) return fail(RA_ERR_INVALID_ARG, "kv_segment_ids is not 16-byte aligned");
+  if ((s = ring_offsets(c, q_pos0, k_pos0, stride, S, &x->qoff, &x->koff)) != RA_OK) return s;
+  if (stride > 1 && c == 1) p->causal = 1;
+  x->kseg = kseg;
+  x->vlog = t_vlog;
+  x->vlog_cap = t_vlog_cap;
+  return RA_OK;
+}
+
+}  // namespace
+
+RA_API ra_status ra_ring_fwd_step(const void* q, const void* k, const void* v, const int32_t* q_segment_ids,
+                                  const int32_t* kv_segment_ids, int causal_block_size, long long q_pos0,
+                                  long long k_pos0, int pos_stride, int batch, int block_len, int heads, int head_dim,
+                                  ra_dtype dtype, float* o_carry, float* lse_carry, void* stream) {
+  const void* ptrs[] = {q, k, v, o_carry, lse_carry};
+  const char* names[] = {"q", "k", "v", "o_carry", "lse_carry"};
+  FwdArgs a;
+  ra_status s = ring_common(ptrs, names, 5, q_segment_ids, kv_segment_ids, causal_block_size, q_pos0, k_pos0,
+                            pos_stride, batch, block_len, heads, head_dim, dtype, &a.p, &a);
+  if (s != RA_OK) return s;
+  if (block_len == 0) return ok();
+  Ctx c;
+  if ((s = make_ctx(stream, &c)) != RA_OK) return s;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = nullptr;
+  a.lse = nullptr;
+  a.o_carry = o_carry;
+  a.lse_carry = lse_carry;
+  uint64_t n = 0;
+  const char* why = nullptr;
+  cudaError_t e = launch_fwd_bf16(a, c, &n, &why);
+  g_launches += n;
+  if (why) return fail(RA_ERR_UNSUPPORTED, "%s", why);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "ring forward step launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+RA_API size_t ra_ring_bwd_workspace_size(int batch, int block_len, int heads, int head_dim, ra_dtype dtype) {
+  if (dtype != RA_BF16) return 0;
+  return ra_bwd_workspace_size(batch, block_len, heads, head_dim, dtype);
+}
+
+namespace {
+
+ra_status ring_bwd_launch(BwdArgs& a, void* workspace, size_t workspace_bytes, void* stream) {
+  const Problem& p = a.p;
+  const size_t need = bwd_workspace_bytes(p.B, p.S, p.H, p.D);
+  if (workspace_bytes < need)
+    return fail(RA_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", workspace_bytes, need);
+  if (p.S == 0) return ok();
+  Ctx c;
+  ra_status s = make_ctx(stream, &c);
+  if (s != RA_OK) return s;
+  a.dq_accum = (float*)workspace;
+  a.delta = (float*)((char*)workspace + bwd_delta_offset(p.B, p.S, p.H, p.D));
+  a.unit_counter = (int*)((char*)workspace + bwd_counter_offset(p.B, p.S, p.H, p.D));
+  uint64_t n = 0;
+  const char* why = nullptr;
+  cudaError_t e = launch_bwd_bf16(a, c, &n, &why);
+  g_launches += n;
+  if (why) return fail(RA_ERR_UNSUPPORTED, "%s", why);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "ring backward launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+RA_API ra_status ra_ring_bwd_begin(const void* out, const float* lse, const void* dout, int batch, int block_len,
+                                   int heads, int head_dim, ra_dtype dtype, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  const void* ptrs[] = {out, lse, dout, workspace};
+  const char* names[] = {"out", "lse", "dout", "workspace"};
+  BwdArgs a;
+  ra_status s = ring_common(ptrs, names, 4, nullptr, nullptr, 0, 0, 0, 1, batch, block_len, heads, head_dim, dtype,
+                            &a.p, &a);
+  if (s != RA_OK) return s;
+  a.stage = kBwdRingBegin;
+  a.out = out;
+  a.lse = lse;
+  a.dout = dout;
+  return ring_bwd_launch(a, workspace, workspace_bytes, stream);
+}
+
+RA_API ra_status ra_ring_bwd_step(const void* q, const void* k, const void* v, const void* dout,
+                                  const int32_t* q_segment_ids, const int32_t* kv_segment_ids, int causal_block_size,
+                                  long long q_pos0, long long k_pos0, int pos_stride, int batch, int block_len,
+                                  int heads, int head_dim, ra_dtype dtype, float* dk_carry, float* dv_carry,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  const void* ptrs[] = {q, k, v, dout, dk_carry, dv_carry, workspace};
+  const char* names[] = {"q", "k", "v", "dout", "dk_carry", "dv_carry", "workspace"};
+  BwdArgs a;
+  ra_status s = ring_common(ptrs, names, 7, q_segment_ids, kv_segment_ids, causal_block_size, q_pos0, k_pos0,
+                            pos_stride, batch, block_len, heads, head_dim, dtype, &a.p, &a);
+  if (s != RA_OK) return s;
+  a.stage = kBwdRingStep;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.dout = dout;
+  a.dk_carry = dk_carry;
+  a.dv_carry = dv_carry;
+  return ring_bwd_launch(a, workspace, workspace_bytes, stream);
+}
+
+RA_API ra_status ra_ring_bwd_end(void* workspace, size_t workspace_bytes, int batch, int block_len, int heads,
+                                 int head_dim, ra_dtype dtype, void* dq, void* stream) {
+  const void* ptrs[] = {workspace, dq};
+  const char* names[] = {"workspace", "dq"};
+  BwdArgs a;
+  ra_status s = ring_common(ptrs, names, 2, nullptr, nullptr, 0, 0, 0, 1, batch, block_len, heads, head_dim, dtype,
+                            &a.p, &a);
+  if (s != RA_OK) return s;
+  a.stage = kBwdRingEnd;
+  a.dq = dq;
+  return ring_bwd_launch(a, workspace, workspace_bytes, stream);
+}
+
+RA_API ra_status ra_ring_finish(const float* src, void* dst, size_t count, ra_dtype dtype, void* stream) {
+  if (dtype != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "ra_ring_finish writes bf16 only");
+  if (count == 0) return ok();
+  if (src == nullptr || dst == nullptr) return fail(RA_ERR_INVALID_ARG, "src or dst is NULL");
+  if (!aligned16(src) || !aligned16(dst)) return fail(RA_ERR_INVALID_ARG, "src and dst must be 16-byte aligned");
+  if (count % 4 != 0) return fail(RA_ERR_INVALID_ARG, "count must be a multiple of 4, got %zu", count);
+  Ctx c;
+  ra_status s = make_ctx(stream, &c);
+  if (s != RA_OK) return s;
+  uint64_t n = 0;
+  cudaError_t e = launch_cast_bf16(src, dst, count, 1.0f, c, &n);
+  g_launches += n;
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "ring finish launch: %s", cudaGetErrorString(e));
   return ok();
 }

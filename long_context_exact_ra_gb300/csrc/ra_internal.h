@@ -18,17 +18,38 @@ struct Problem {
   const int32_t* seg;  // [B, S] or nullptr
 };
 
-struct FwdArgs {
+// Optional extras shared by the forward and backward calls.
+struct CallExtras {
+  // Positions: query row r sits at r + qoff, key row x at x + koff (see the
+  // ring-step entry points); kseg = key rows' segment ids (null: p.seg).
+  int qoff = 0, koff = 0;
+  const int32_t* kseg = nullptr;
+  int* vlog = nullptr;  // debug visit log (ra_debug_visitlog), or null
+  int vlog_cap = 0;     // entries it holds
+};
+
+struct FwdArgs : CallExtras {
   Problem p;
   const void* q;
   const void* k;
   const void* v;
   void* out;
   float* lse;
+  float* o_carry = nullptr;    // ring step: fp32 running output (then out/lse are unused)
+  float* lse_carry = nullptr;  // ring step: running lse
 };
 
-struct BwdArgs {
+// What a backward call runs.
+enum BwdStage : int {
+  kBwdWhole = 0,      // preprocess, main kernel, finalize (ra_bwd)
+  kBwdRingBegin = 1,  // preprocess only (Delta, lse*log2(e); dQ accumulator zeroed)
+  kBwdRingStep = 2,   // main kernel with fp32 dK/dV carries
+  kBwdRingEnd = 3,    // finalize only (dq from the accumulator)
+};
+
+struct BwdArgs : CallExtras {
   Problem p;
+  int stage = kBwdWhole;
   const void* q;
   const void* k;
   const void* v;
@@ -41,6 +62,8 @@ struct BwdArgs {
   float* dq_accum;  // [B, S, H, D] fp32 scratch (bf16 path)
   float* delta;     // fp32 path: [B, H, S] Delta; bf16 path: float2 (lse*log2(e), Delta) rows of bwd_row_pitch
   int* unit_counter;  // bf16 path: the main kernel's unit counter (in the workspace)
+  float* dk_carry = nullptr;  // ring step: fp32 dK accumulator of the key/value block
+  float* dv_carry = nullptr;  // ring step: fp32 dV accumulator
 };
 
 // Launch context: device facts and the device status word.
@@ -99,6 +122,9 @@ cudaError_t launch_bwd_f32(const BwdArgs& a, const Ctx& c, uint64_t* launches);
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const Ctx& c, uint64_t* launches, const char** why);
 cudaError_t launch_bwd_bf16(const BwdArgs& a, const Ctx& c, uint64_t* launches, const char** why);
 cudaError_t launch_selftest_timeout(const Ctx& c, uint64_t* launches);
+// dst[i] = bf16(src[i] * scale), i < count (count a multiple of 4, both 16-byte aligned).
+cudaError_t launch_cast_bf16(const float* src, void* dst, size_t count, float scale, const Ctx& c,
+                             uint64_t* launches);
 
 // Sets the calling thread's ra_last_error() message and returns s.
 ra_status set_last_error(ra_status s, const char* msg);

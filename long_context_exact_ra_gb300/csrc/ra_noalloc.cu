@@ -15,7 +15,6 @@
 // at zero (the fp32 dQ accumulator) on every call.  Calls whose work overlaps
 // on the GPU (different streams, no ordering between them) race on the array.
 #include <cstdio>
-#include <mutex>
 
 #include "ra.h"
 #include "ra_internal.h"
@@ -27,29 +26,21 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[RA_NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_mu;
-void* g_ptr[256];
-
-// Device address of the scratch array on the current device (set up once per
-// device, with that device current).  In host code `g_bwd_scratch` names a host
+// Device address of the scratch array on the current device, looked up on every
+// call with that device current.  In host code `g_bwd_scratch` names a host
 // stand-in, not device memory, so only this address may be passed to kernels.
+// The lookup is not cached: after a device reset the array is loaded again at
+// a new address, and a cached one would point at memory the library no longer
+// owns.  Once the array is loaded the lookup allocates nothing.
 ra_status scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return set_last_error(RA_ERR_CUDA, cudaGetErrorString(e));
-  if (dev < 0 || dev >= 256) return set_last_error(RA_ERR_CUDA, "device ordinal out of range");
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_bwd_scratch);
-    if (e != cudaSuccess) {
-      char msg[256];
-      snprintf(msg, sizeof(msg), "cudaGetSymbolAddress(no-alloc scratch): %s", cudaGetErrorString(e));
-      return set_last_error(RA_ERR_CUDA, msg);
-    }
-    g_ptr[dev] = p;
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_bwd_scratch);
+  if (e != cudaSuccess) {
+    char msg[256];
+    snprintf(msg, sizeof(msg), "cudaGetSymbolAddress(no-alloc scratch): %s", cudaGetErrorString(e));
+    return set_last_error(RA_ERR_CUDA, msg);
   }
-  *out = g_ptr[dev];
+  *out = p;
   return RA_OK;
 }
 

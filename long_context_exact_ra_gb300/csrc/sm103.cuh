@@ -289,6 +289,24 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// Debug visit log: the caller's device buffer of int32 words.  Word 0 counts the
+// entries claimed (it keeps counting past the capacity, so overflow shows);
+// words 1-7 are reserved; entry e occupies words 8 + 8e .. 8e + 15:
+//   kind (0 forward, 1 backward) | CTA index << 8, batch, head, the unit's home
+//   shard, the unit's tile in that shard, ring step, visited shard, visited tile
+//   in that shard.
+// One producer lane claims the entries of its unit in visit order, so sorting a
+// unit's entries by position gives the order in which it visited the tiles.
+__device__ __forceinline__ void visit_log(int* log, int cap, int kind, int b, int h, int home_shard, int home_tile,
+                                          int step, int vshard, int vtile) {
+  const int e = atomicAdd(log, 1);
+  if (e < cap) {
+    int4* p = reinterpret_cast<int4*>(log + 8 + 8 * (size_t)e);
+    p[0] = make_int4(kind | ((int)blockIdx.x << 8), b, h, home_shard);
+    p[1] = make_int4(home_tile, step, vshard, vtile);
+  }
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

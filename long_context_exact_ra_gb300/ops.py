@@ -21,7 +21,9 @@ _STATUS = {1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "device 
 
 EXPORTS = ("ra_fwd", "ra_bwd", "ra_bwd_workspace_size", "ra_sync_check", "ra_last_error",
            "ra_kernel_launches", "ra_selftest_timeout", "ra_bwd_noalloc", "ra_bwd_noalloc_max_scratch",
-           "ra_decode", "ra_decode_workspace_size", "ra_blockwise_ffn", "ra_ffn_workspace_size")
+           "ra_decode", "ra_decode_workspace_size", "ra_blockwise_ffn", "ra_ffn_workspace_size",
+           "ra_debug_visitlog", "ra_ring_fwd_step", "ra_ring_bwd_workspace_size", "ra_ring_bwd_begin",
+           "ra_ring_bwd_step", "ra_ring_bwd_end", "ra_ring_finish")
 
 
 class RAError(RuntimeError):
@@ -70,6 +72,22 @@ def lib() -> ctypes.CDLL:
     L.ra_ffn_workspace_size.argtypes = [i32, i32, i32, i32]
     L.ra_blockwise_ffn.restype = i32
     L.ra_blockwise_ffn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp]
+    i64 = ctypes.c_longlong
+    L.ra_debug_visitlog.restype = i32
+    L.ra_debug_visitlog.argtypes = [vp, sz]
+    L.ra_ring_fwd_step.restype = i32
+    L.ra_ring_fwd_step.argtypes = [vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    L.ra_ring_bwd_workspace_size.restype = sz
+    L.ra_ring_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    L.ra_ring_bwd_begin.restype = i32
+    L.ra_ring_bwd_begin.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, sz, vp]
+    L.ra_ring_bwd_step.restype = i32
+    L.ra_ring_bwd_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, i32, i32, i32, vp, vp,
+                                   vp, sz, vp]
+    L.ra_ring_bwd_end.restype = i32
+    L.ra_ring_bwd_end.argtypes = [vp, sz, i32, i32, i32, i32, i32, vp, vp]
+    L.ra_ring_finish.restype = i32
+    L.ra_ring_finish.argtypes = [vp, vp, sz, i32, vp]
     _lib = L
     return L
 
@@ -108,6 +126,13 @@ def _check_tensor(name, t, like=None, dtype=None):
         raise ValueError(f"{name} must be {dtype}")
 
 
+def _check_segment_ids(segment_ids, B, S):
+    if segment_ids is not None:
+        _check_tensor("segment_ids", segment_ids, dtype=torch.int32)
+        if tuple(segment_ids.shape) != (B, S):
+            raise ValueError("segment_ids must be [batch, seq]")
+
+
 def _chunks(S, num_shards, query_chunk_size, key_chunk_size):
     ssh = S // num_shards if num_shards > 0 else 0
     qc = query_chunk_size if query_chunk_size is not None else max(ssh, 1)
@@ -122,10 +147,7 @@ def fwd(q, k, v, segment_ids=None, causal_block_size=0, num_shards=1,
     _check_tensor("k", k, q)
     _check_tensor("v", v, q)
     B, S, H, D = q.shape
-    if segment_ids is not None:
-        _check_tensor("segment_ids", segment_ids, dtype=torch.int32)
-        if tuple(segment_ids.shape) != (B, S):
-            raise ValueError("segment_ids must be [batch, seq]")
+    _check_segment_ids(segment_ids, B, S)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -152,8 +174,7 @@ def bwd(q, k, v, out, lse, dout, segment_ids=None, causal_block_size=0, num_shar
         _check_tensor(name, t, q)
     _check_tensor("lse", lse, dtype=torch.float32)
     B, S, H, D = q.shape
-    if segment_ids is not None:
-        _check_tensor("segment_ids", segment_ids, dtype=torch.int32)
+    _check_segment_ids(segment_ids, B, S)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
@@ -176,8 +197,7 @@ def bwd_noalloc(q, k, v, out, lse, dout, segment_ids=None, causal_block_size=0, 
         _check_tensor(name, t, q)
     _check_tensor("lse", lse, dtype=torch.float32)
     B, S, H, D = q.shape
-    if segment_ids is not None:
-        _check_tensor("segment_ids", segment_ids, dtype=torch.int32)
+    _check_segment_ids(segment_ids, B, S)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
@@ -274,3 +294,91 @@ def kernel_launches() -> int:
 
 def selftest_timeout(limit_ns: int, stream=None):
     _check(lib().ra_selftest_timeout(int(limit_ns), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- debug visit log
+VISITLOG_HEADER_WORDS = 8
+VISITLOG_ENTRY_WORDS = 8
+
+
+def debug_visitlog(buf):
+    """ra_debug_visitlog: make the calling thread's next bf16 attention calls record
+    the tiles their kernels visit into `buf` (int32 CUDA tensor; word 0 counts the
+    entries, which start at word 8, 8 words each), or stop recording (buf=None)."""
+    if buf is not None:
+        _check_tensor("visit log", buf, dtype=torch.int32)
+    _check(lib().ra_debug_visitlog(_ptr(buf), 0 if buf is None else buf.numel()))
+
+
+# ----------------------------------------------------------------------------- ring steps
+def _ring_seg(q_segment_ids, kv_segment_ids, B, S):
+    if (q_segment_ids is None) != (kv_segment_ids is None):
+        raise ValueError("q_segment_ids and kv_segment_ids must be given together")
+    _check_segment_ids(q_segment_ids, B, S)
+    _check_segment_ids(kv_segment_ids, B, S)
+
+
+def ring_fwd_step(q, k, v, q_segment_ids, kv_segment_ids, causal_block_size, q_pos0, k_pos0, pos_stride,
+                  o_carry, lse_carry, stream=None):
+    """ra_ring_fwd_step: merge attention(q block, k/v block) into (o_carry fp32 [B,S,H,D], lse_carry [B,H,S])."""
+    _check_tensor("q", q)
+    _check_tensor("k", k, q)
+    _check_tensor("v", v, q)
+    B, S, H, D = q.shape
+    _ring_seg(q_segment_ids, kv_segment_ids, B, S)
+    _check_tensor("o_carry", o_carry, dtype=torch.float32)
+    _check_tensor("lse_carry", lse_carry, dtype=torch.float32)
+    if tuple(o_carry.shape) != (B, S, H, D) or tuple(lse_carry.shape) != (B, H, S):
+        raise ValueError("o_carry must be [B, S, H, D] and lse_carry [B, H, S]")
+    _check(lib().ra_ring_fwd_step(_ptr(q), _ptr(k), _ptr(v), _ptr(q_segment_ids), _ptr(kv_segment_ids),
+                                  int(causal_block_size), int(q_pos0), int(k_pos0), int(pos_stride), B, S, H, D,
+                                  _dtype_code(q), _ptr(o_carry), _ptr(lse_carry), _stream(stream)))
+
+
+def ring_bwd_workspace_size(B, S, H, D) -> int:
+    return int(lib().ra_ring_bwd_workspace_size(B, S, H, D, RA_BF16))
+
+
+def ring_bwd_begin(out, lse, dout, workspace, stream=None):
+    """ra_ring_bwd_begin: Delta and the zeroed dQ accumulator of this query block, in `workspace`."""
+    _check_tensor("out", out)
+    _check_tensor("dout", dout, out)
+    _check_tensor("lse", lse, dtype=torch.float32)
+    B, S, H, D = out.shape
+    _check(lib().ra_ring_bwd_begin(_ptr(out), _ptr(lse), _ptr(dout), B, S, H, D, _dtype_code(out), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def ring_bwd_step(q, k, v, dout, q_segment_ids, kv_segment_ids, causal_block_size, q_pos0, k_pos0, pos_stride,
+                  dk_carry, dv_carry, workspace, stream=None):
+    """ra_ring_bwd_step: add this (query block, key/value block) pair's gradients: dQ into the
+    workspace accumulator, dK and dV into the fp32 carries of the key/value block."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        _check_tensor(name, t, q)
+    B, S, H, D = q.shape
+    _ring_seg(q_segment_ids, kv_segment_ids, B, S)
+    for name, t in (("dk_carry", dk_carry), ("dv_carry", dv_carry)):
+        _check_tensor(name, t, dtype=torch.float32)
+        if tuple(t.shape) != (B, S, H, D):
+            raise ValueError(f"{name} must be [B, S, H, D]")
+    _check(lib().ra_ring_bwd_step(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(q_segment_ids), _ptr(kv_segment_ids),
+                                  int(causal_block_size), int(q_pos0), int(k_pos0), int(pos_stride), B, S, H, D,
+                                  _dtype_code(q), _ptr(dk_carry), _ptr(dv_carry), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def ring_bwd_end(workspace, dq, stream=None):
+    """ra_ring_bwd_end: dq (like q) from the workspace's dQ accumulator."""
+    _check_tensor("dq", dq)
+    B, S, H, D = dq.shape
+    _check(lib().ra_ring_bwd_end(_ptr(workspace), workspace.numel() * workspace.element_size(), B, S, H, D,
+                                 _dtype_code(dq), _ptr(dq), _stream(stream)))
+
+
+def ring_finish(src, dst, stream=None):
+    """ra_ring_finish: dst (bf16) = src (fp32), element by element."""
+    _check_tensor("src", src, dtype=torch.float32)
+    _check_tensor("dst", dst, dtype=torch.bfloat16)
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst must have the same number of elements")
+    _check(lib().ra_ring_finish(_ptr(src), _ptr(dst), src.numel(), RA_BF16, _stream(stream)))

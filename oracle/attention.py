@@ -31,7 +31,8 @@ Sources (web pages on Ring Attention; cited by page title and section):
       q_chunk_idx_start + q_chunk_idx, query_chunk_size,
       k_chunk_idx_start + k_chunk_idx, key_chunk_size, causal_block_size).
 
-Readings where the pages are silent (each is also listed in the design notes):
+Readings where the pages are silent (the plainest reading that the rest of
+the pages supports):
 
 * visible(i, j) = (c == 0 or i // c >= j // c) and (no segments or
   seg[i] == seg[j]), c = causal_block_size.  The body of below_or_on_diag is

@@ -21,7 +21,8 @@ Sources (cited by page title and section):
   page), §2 数值稳定的注意力计算: the lazy-softmax running max / numerator /
   denominator update that merges the per-block results.
 
-Readings where the pages are silent (each is also listed in the design notes):
+Readings where the pages are silent (the plainest reading that the rest of
+the pages supports):
 
 * ``cache_idx[b]`` is the number of cache entries of batch row b that precede
   the new tokens: new token t sits at position ``cache_idx[b] + t``, and its

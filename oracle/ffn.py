@@ -15,7 +15,7 @@ Sources (cited by page title and section):
   feed-forward runs on one chunk at a time (only that chunk's hidden
   activation exists at once), and the chunk results are put back in order.
 
-Readings (also listed in the design notes):
+Readings where the pages leave the point open:
 
 * Weights are stored the way a linear layer stores them: w1 is [F, Dm] (W1
   transposed) and w2 is [Dm, F] (W2 transposed), so x W1 = x @ w1.T.  Biases

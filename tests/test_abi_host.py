@@ -138,3 +138,34 @@ def test_ffn_validation_and_workspace(L):
     assert L.ra_ffn_workspace_size(2, 1000, 128, 512) == 512 * 128 * 2
     assert L.ra_ffn_workspace_size(1, 100, 128, 512) == 100 * 128 * 2
     assert L.ra_ffn_workspace_size(0, 100, 128, 512) == 0
+
+
+def test_ring_step_and_visit_log_validation(L):
+    """Rejections that happen before any CUDA call."""
+    P = ctypes.c_void_p
+    a = P(256)
+
+    def fwd_step(c=1, q0=0, k0=0, stride=1, dt=ops.RA_BF16, qseg=None, kseg=None, S=128, D=64, o=a):
+        return L.ra_ring_fwd_step(a, a, a, qseg, kseg, c, q0, k0, stride, 1, S, 1, D, dt, o, a, None)
+
+    assert fwd_step(c=3, q0=1, k0=0, stride=4) == ops.RA_ERR_UNSUPPORTED       # strided + block causal
+    assert b"strided" in L.ra_last_error()
+    assert fwd_step(q0=-1) == ops.RA_ERR_INVALID_ARG
+    assert fwd_step(stride=0) == ops.RA_ERR_INVALID_ARG
+    assert fwd_step(k0=1 << 30) == ops.RA_ERR_INVALID_ARG                       # positions below 2^30
+    assert fwd_step(dt=ops.RA_F32) == ops.RA_ERR_UNSUPPORTED                    # bf16 only
+    assert fwd_step(qseg=P(512)) == ops.RA_ERR_INVALID_ARG                      # both ids or neither
+    assert fwd_step(o=None) == ops.RA_ERR_INVALID_ARG
+    assert fwd_step(D=96) == ops.RA_ERR_UNSUPPORTED
+    assert L.ra_ring_bwd_step(a, a, a, a, None, None, 1, 0, 0, 1, 1, 128, 1, 64, ops.RA_BF16, a, a, a, 16,
+                              None) == ops.RA_ERR_INVALID_ARG                    # workspace too small
+    assert b"workspace" in L.ra_last_error()
+    assert L.ra_ring_bwd_workspace_size(1, 128, 1, 64, ops.RA_BF16) == L.ra_bwd_workspace_size(1, 128, 1, 64,
+                                                                                               ops.RA_BF16)
+    assert L.ra_ring_finish(a, a, 6, ops.RA_BF16, None) == ops.RA_ERR_INVALID_ARG  # count % 4
+    assert L.ra_ring_finish(a, a, 8, ops.RA_F32, None) == ops.RA_ERR_UNSUPPORTED
+    assert L.ra_ring_finish(a, a, 0, ops.RA_BF16, None) == ops.RA_OK              # nothing to do
+    # visit log: alignment and size rules; NULL turns it off
+    assert L.ra_debug_visitlog(P(260), 64) == ops.RA_ERR_INVALID_ARG
+    assert L.ra_debug_visitlog(a, 15) == ops.RA_ERR_INVALID_ARG
+    assert L.ra_debug_visitlog(None, 0) == ops.RA_OK

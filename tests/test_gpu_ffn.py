@@ -11,12 +11,22 @@ from tests.gpu_util import host_f64
 
 pytestmark = pytest.mark.gpu
 
-# Tolerance: the output is rounded to bf16 (2^-9 relative) and the hidden
-# activation is rounded to bf16 on both sides from pre-activations that differ
-# by fp32 accumulation error, so a hidden value can land one bf16 step apart
-# (2^-8 relative); through w2 ~ N(0, 1/F) that stays far below 1e-2.
-FFN_MAX_REL = 1e-2   # max |err| / max(1, |ref|)
+# Two oracles.  The exact one is the definition FFN(x) = max(0, x W1 + b1) W2 + b2
+# in float64 (paper review page; blockwise feed-forward page, §核心技术原理).
+# bf16 keeps 8 significant bits: rounding moves a value by at most 2^-8 of itself,
+# by about 2^-9 of itself in rms.  The kernel rounds twice:
+#   * the output, at most 2^-8 |y|;
+#   * the hidden activation, which it stores in bf16 between the two products.
+#     Through w2 ~ N(0, 1/F) that moves an output by a sum of F small terms of
+#     random sign, sigma ~ 2^-9 x rms(hidden) ~ 1.4e-3 (the hidden rms is ~0.7).
+# Bound against the exact definition: 2^-8 + 8 sigma ~ 1.5e-2 relative to
+# max(1, |y|); the mean stays near 1.3e-3 (a float64 model of the two roundings
+# gives max 0.009 and mean 0.0013 on these shapes).  The emulating oracle rounds
+# the hidden activation as the kernel stores it, which leaves the output's own
+# rounding (2^-8) and fp32 accumulation order: a bound of 5e-3.
+FFN_MAX_REL = 1.5e-2   # max |err| / max(1, |ref|), against the exact definition
 FFN_MEAN_ABS = 2e-3
+FFN_EMU_MAX_REL = 5e-3  # against the oracle that rounds the hidden activation as the kernel stores it
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -40,11 +50,11 @@ def run(xi, chunk=None):
     return out, ops.kernel_launches() - before
 
 
-def check(got, ref):
+def check(got, ref, max_rel=FFN_MAX_REL, what="exact"):
     err = np.abs(got - ref)
     rel = (err / np.maximum(1.0, np.abs(ref))).max()
-    assert rel <= FFN_MAX_REL, f"max rel err {rel:.3e}"
-    assert err.mean() <= FFN_MEAN_ABS, f"mean abs err {err.mean():.3e}"
+    assert rel <= max_rel, f"{what}: max rel err {rel:.3e}"
+    assert err.mean() <= FFN_MEAN_ABS, f"{what}: mean abs err {err.mean():.3e}"
 
 
 SMALL = [
@@ -62,10 +72,11 @@ def test_ffn_small_full(B, L, Dm, F, chunk, bias):
     xi = make_ffn_inputs(FfnWorkload("ffn small", B, L, Dm, F, chunk, seed=L + F, bias=bias))
     out, launches = run(xi)
     assert launches == 2 * ((B * L + chunk - 1) // chunk)
-    ref = oracle.ref_blockwise_ffn(xi.as_f64("x"), xi.as_f64("w1"), xi.as_f64("b1") if bias else np.zeros(F),
-                                   xi.as_f64("w2"), xi.as_f64("b2") if bias else np.zeros(Dm), chunk,
-                                   round_hidden_bf16=True)
-    check(host_f64(out), ref)
+    args = (xi.as_f64("x"), xi.as_f64("w1"), xi.as_f64("b1") if bias else np.zeros(F),
+            xi.as_f64("w2"), xi.as_f64("b2") if bias else np.zeros(Dm), chunk)
+    got = host_f64(out)
+    check(got, oracle.ref_blockwise_ffn(*args, round_hidden_bf16=False))
+    check(got, oracle.ref_blockwise_ffn(*args, round_hidden_bf16=True), FFN_EMU_MAX_REL, "emulated")
 
 
 def test_ffn_chunk_size_does_not_change_the_result():
@@ -87,6 +98,7 @@ def test_ffn_7b_sampled_rows():
     rows = sorted({0, 1, 127, 128, w.chunk_size - 1, w.chunk_size, w.chunk_size + 1, w.seq - 1}
                   | set(g.integers(w.seq, size=40).tolist()))
     x = xi.as_f64("x")[0, rows]
-    ref = oracle.ffn_rows(x, xi.as_f64("w1"), xi.as_f64("b1"), xi.as_f64("w2"), xi.as_f64("b2"),
-                          round_hidden_bf16=True)
-    check(host_f64(out)[0, rows], ref)
+    args = (x, xi.as_f64("w1"), xi.as_f64("b1"), xi.as_f64("w2"), xi.as_f64("b2"))
+    got = host_f64(out)[0, rows]
+    check(got, oracle.ffn_rows(*args, round_hidden_bf16=False))
+    check(got, oracle.ffn_rows(*args, round_hidden_bf16=True), FFN_EMU_MAX_REL, "emulated")

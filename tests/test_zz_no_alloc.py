@@ -73,3 +73,20 @@ def test_noalloc_rejects_problems_beyond_the_scratch_array():
     st = L.ra_bwd_noalloc(P, P, P, P, P, P, None, 1, 8, 1024, 1024, B, S, H, D, ops.RA_BF16, P, P, P, None)
     assert st == ops.RA_ERR_INVALID_ARG
     assert b"scratch" in L.ra_last_error()
+
+
+def test_noalloc_fp32_path_through_the_binding_matches_ra_bwd_twice():
+    """The fp32 path (the scratch holds only Delta there) through ops.bwd_noalloc."""
+    w = Workload("no-alloc fp32", 1, 512, 2, 64, "f32", 0, 4, 128, 128, backward=True, seed=17)
+    x = make_inputs(w, with_dout=True)
+    q, k, v, do = (to_dev(getattr(x, n), "f32") for n in ("q", "k", "v", "dout"))
+    args = (None, w.causal_block_size, w.num_shards, w.query_chunk_size, w.key_chunk_size)
+    out, lse = ops.fwd(q, k, v, *args)
+    ref = [host_f64(t) for t in ops.bwd(q, k, v, out, lse, do, *args)]
+    ops.sync_check()
+    for call in range(2):
+        got = ops.bwd_noalloc(q, k, v, out, lse, do, *args)
+        ops.sync_check()
+        for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+            rel = (np.abs(host_f64(g) - r) / np.maximum(1.0, np.abs(r))).max()
+            assert rel <= 1e-5, f"call {call}: {name}: max rel err {rel:.3e}"
