@@ -10,6 +10,7 @@ host memory) through `ring_forward` / `ring_backward`.  The kernels of the two
 processes never wait on each other: every exchange happens on the host between
 launches.  Tolerances are those of the single-launch path.
 """
+import datetime
 import os
 import socket
 import sys
@@ -105,7 +106,7 @@ def _two_rank_worker(rank, world, port, layout, result_q):
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=120))
     torch.cuda.set_device(0)
     from long_context_exact_ra_gb300 import ring as rg
 
@@ -144,7 +145,7 @@ def test_two_ranks_on_one_gpu_host_staged(layout):
     world, port = 2, _free_port()
     ctx = mp.get_context("spawn")
     qq = ctx.Queue()
-    procs = [ctx.Process(target=_two_rank_worker, args=(r, world, port, layout, qq)) for r in range(world)]
+    procs = [ctx.Process(target=_two_rank_worker, args=(r, world, port, layout, qq), daemon=True) for r in range(world)]
     for p in procs:
         p.start()
     res = sorted((qq.get(timeout=300) for _ in range(world)), key=lambda t: t[0])

@@ -7,6 +7,7 @@ contiguous and striped blocks, causal or not, with and without segment ids:
 the ring order, the exchange and the position bookkeeping are then right
 (paper review page of Ring Attention, 环形通信 / 环形注意力算法; the result does
 not depend on the block order, 排列不变性)."""
+import datetime
 import os
 import socket
 import sys
@@ -52,7 +53,7 @@ def _inputs(seed, B=2, S=48, H=2, D=8, segments=False):
 def _worker(rank, ws, port, layout, c, segments, q_out):
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
-    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    dist.init_process_group("gloo", rank=rank, world_size=ws, timeout=datetime.timedelta(seconds=120))
     from long_context_exact_ra_gb300 import ring
     from tests.ring_fake import Float64RingKernels
     q, k, v, do, seg = (None if a is None else torch.from_numpy(a) for a in _inputs(ws * 10 + c, segments=segments))
@@ -73,7 +74,7 @@ def test_ring_driver_on_gloo_ranks_matches_the_oracle(world, layout, c, segments
     port = _free_port()
     ctx = mp.get_context("spawn")
     qq = ctx.Queue()
-    procs = [ctx.Process(target=_worker, args=(r, world, port, layout, c, segments, qq)) for r in range(world)]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, layout, c, segments, qq), daemon=True) for r in range(world)]
     for p in procs:
         p.start()
     res = sorted((qq.get(timeout=120) for _ in range(world)), key=lambda t: t[0])
