@@ -612,7 +612,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               vis &= (cb <= 0) | ((qidx + (kCarry ? P.qoff : 0)) / max(cb, 1) >= kblk);
               const int qs = qsegp ? __ldg(qsegp + min(qidx, pb.S - 1)) : kseg;
               vis &= (qs == kseg);
+              // masked: P = 0 and dS = 0 (dS by a select too, not 0 * (dP - Delta): the
+              // (lse, Delta) entries of columns past the sequence end are not written)
               pq[y] = vis ? pq[y] : 0.f;
+              dq16[y] = vis ? dq16[y] : 0.f;
             }
           }
           uint32_t pk[8], dk[8];

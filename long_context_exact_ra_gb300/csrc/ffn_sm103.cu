@@ -54,6 +54,7 @@ struct GemmParams {
   int M, N, K;      // rows of this launch, output columns, reduction length
   int a_row0;       // first row of A inside its tensor map
   int tiles_m, tiles_n;
+  int group_n;        // column tiles per raster group (see tile_coords)
   const float* bias;  // [N] or nullptr
   __nv_bfloat16* c;   // row-major, leading dimension ldc
   long long ldc;
@@ -69,6 +70,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(map), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
+}
+
+// Tile t -> (first row, first column).  Tiles go in groups of group_n column
+// tiles: inside a group the column tile varies fastest and the row tiles follow
+// one another, so the group's columns of B (group_n x 256 rows of the weight
+// matrix) stay in L2 while the rows of A stream through once per group, and the
+// CTAs running at the same time share each A row tile.
+__device__ __forceinline__ void tile_coords(const GemmParams& P, int t, int& m0, int& n0) {
+  const int per_group = P.tiles_m * P.group_n;
+  const int g = t / per_group, w = t - g * per_group;
+  const int gn0 = g * P.group_n;
+  const int gw = min(P.group_n, P.tiles_n - gn0);  // the last group may be narrower
+  m0 = (w / gw) * kGM;
+  n0 = (gn0 + w % gw) * kGN;
 }
 
 __global__ void __launch_bounds__(kGThreads, 1)
@@ -120,7 +135,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
       int it = 0;
       bool alive = true;
       for (int t = blockIdx.x; t < tiles && alive; t += gridDim.x) {
-        const int m0 = (t % P.tiles_m) * kGM, n0 = (t / P.tiles_m) * kGN;
+        int m0, n0;
+        tile_coords(P, t, m0, n0);
         for (int kb = 0; kb < ksteps; ++kb) {
           const int s = it % kGST;
           alive = mbar_wait(empty(s), ((it / kGST) & 1) ^ 1, ctl, 80);
@@ -182,7 +198,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const bool ok = __all_sync(0xffffffffu, mbar_wait(accfull(a), (ti >> 1) & 1, ctl, 84));
       if (!ok) break;
       tc_fence_after();
-      const int m0 = (t % P.tiles_m) * kGM, n0 = (t / P.tiles_m) * kGN;
+      int m0, n0;
+      tile_coords(P, t, m0, n0);
       const bool row_ok = m0 + row < P.M;
       __nv_bfloat16* crow = P.c + (P.c_row0 + m0 + row) * P.ldc;
 #pragma unroll 1
@@ -275,6 +292,10 @@ cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, GemmParams
   }
   P.tiles_m = (P.M + kGM - 1) / kGM;
   P.tiles_n = (P.N + kGN - 1) / kGN;
+  {  // column tiles whose B rows (256 x K bf16 each) fit in 48 MB of L2 together
+    const long long per = (long long)kGN * P.K * 2;
+    P.group_n = (int)std::max(1LL, std::min((long long)P.tiles_n, (48LL << 20) / per));
+  }
   P.status = c.status;
   P.limit_ns = c.limit_ns;
   const int tiles = P.tiles_m * P.tiles_n;

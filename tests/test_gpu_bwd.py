@@ -191,3 +191,29 @@ def test_config5_sampled_rows_and_invariants():
         tol = 8 * 2.0 ** -8 * gnorm + 1e-2
         dev_ = np.abs(gsum - target)
         assert np.all(dev_ <= tol), f"sum of {name} rows: worst {dev_.max():.3e} (bound there {tol.flat[dev_.argmax()]:.3e})"
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_backward_workspace_contents_do_not_matter(D):
+    """ra_bwd_workspace_size's contents on entry do not matter: a workspace full of
+    NaN bit patterns (0xFF bytes) gives the same gradients as a zeroed one.  The
+    shape has a ragged last tile, whose columns past the sequence end read the
+    unwritten tail of the (lse, Delta) rows; the masked tiles must give them P = 0
+    and dS = 0 without multiplying by those entries."""
+    w = Workload("ws contents", 1, 1200, 2, D, "bf16", 1, 4, 100, 100, backward=True, seed=99 + D)
+    x = make_inputs(w, with_dout=True)
+    q, k, v, do = (to_dev(getattr(x, n), "bf16") for n in ("q", "k", "v", "dout"))
+    cargs = (None, 1, 4, 100, 100)
+    out, lse = ops.fwd(q, k, v, *cargs)
+    need = ops.bwd_workspace_size(1, 1200, 2, D, torch.bfloat16)
+    grads = []
+    for fill in (0, 255):
+        ws = torch.full((need,), fill, dtype=torch.uint8, device="cuda")
+        grads.append(ops.bwd(q, k, v, out, lse, do, *cargs, workspace=ws))
+    ops.sync_check()
+    rq, rk, rv = oracle.ref_bwd(*(as_f64(getattr(x, n), "bf16") for n in ("q", "k", "v", "dout")), None, 1)
+    for g in grads:
+        for name, t, r in zip(("dq", "dk", "dv"), g, (rq, rk, rv)):
+            got = host_f64(t)
+            assert np.isfinite(got).all(), name
+            check_grad(got, r, name)
