@@ -220,7 +220,7 @@ __device__ __forceinline__ int bticket_unit(const BwdParams& P, int t) {
 // ---------------------------------------------------------------------------
 // 2. main kernel
 // ---------------------------------------------------------------------------
-template <int D, bool kCarry>
+template <int D, bool kCarry, bool kLog>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               r.k0 = k0;
               r.kvalid = kvalid;
               alive = publish(r);
-              if (P.vlog) visit_log(P.vlog, P.vlog_cap, 1, b, h, k, t, i, js, t0 + tt);
+              if constexpr (kLog) visit_log(P.vlog, P.vlog_cap, 1, b, h, k, t, i, js, t0 + tt);
             }
             alive = __shfl_sync(0xffffffffu, alive, 0);
             ++pair_n;
@@ -766,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Stages of the backward (BwdArgs::stage): the whole backward on one sequence,
 // or one of the three parts a ring of separate blocks runs (begin once,
 // one step per key/value block, end once).
-template <int D, bool kCarry>
+template <int D, bool kCarry, bool kLog>
 static cudaError_t launch_bwd_main(const BwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
   using Cf = BCfg<D>;
   const Problem& p = a.p;
@@ -801,15 +801,15 @@ static cudaError_t launch_bwd_main(const BwdArgs& a, const Ctx& c, uint64_t* lau
     const long long per = 8LL * p.S * p.D;
     P.group_heads = (int)std::max(1LL, std::min((long long)p.B * p.H, (48LL << 20) / per));
   }
-  static std::atomic<bool> attr_set[256][2];  // idempotent attribute; atomic so threads may race
-  if (!attr_set[c.device][kCarry]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(bwd_bf16_kernel<D, kCarry>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM);
+  static std::atomic<bool> attr_set[256];  // idempotent attribute; atomic so threads may race
+  if (!attr_set[c.device]) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_bf16_kernel<D, kCarry, kLog>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Cf::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set[c.device][kCarry] = true;
+    attr_set[c.device] = true;
   }
   const int grid = std::min(c.num_sms, P.num_units);
-  bwd_bf16_kernel<D, kCarry><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, mdo, P);
+  bwd_bf16_kernel<D, kCarry, kLog><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, mdo, P);
   *launches += 1;
   return cudaGetLastError();
 }
@@ -827,12 +827,14 @@ static cudaError_t launch_bwd_bf16_d(const BwdArgs& a, const Ctx& c, uint64_t* l
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.stage == kBwdWhole) {
-    e = launch_bwd_main<D, false>(a, c, launches, why);
+    e = a.vlog ? launch_bwd_main<D, false, true>(a, c, launches, why)
+               : launch_bwd_main<D, false, false>(a, c, launches, why);
     if (e != cudaSuccess || *why) return e;
   } else if (a.stage == kBwdRingStep) {
     // every launch of the main kernel starts from a zero unit counter
     if ((e = cudaMemsetAsync(a.unit_counter, 0, sizeof(int), c.stream)) != cudaSuccess) return e;
-    e = launch_bwd_main<D, true>(a, c, launches, why);
+    e = a.vlog ? launch_bwd_main<D, true, true>(a, c, launches, why)
+               : launch_bwd_main<D, true, false>(a, c, launches, why);
     if (e != cudaSuccess || *why) return e;
   }
   if (a.stage == kBwdWhole || a.stage == kBwdRingEnd) {

@@ -156,7 +156,7 @@ __device__ __forceinline__ int ticket_unit(const FwdParams& P, int t) {
   return (g0 + (w - rank * gh)) * per_head + rank;
 }
 
-template <int D, bool kCarry>
+template <int D, bool kCarry, bool kLog>
 __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-partitions -> <= 168 registers
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const FwdParams P) {
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
               r.qvalid1 = qv1;
               if constexpr (D == 64) r.kseg = kseg;
               alive = publish(r);
-              if (P.vlog) visit_log(P.vlog, P.vlog_cap, 0, b, h, j, pr, i, ks, t0 + tt);
+              if constexpr (kLog) visit_log(P.vlog, P.vlog_cap, 0, b, h, j, pr, i, ks, t0 + tt);
               const int s = tile_n % C::KST;
               const uint32_t par = ((tile_n / C::KST) & 1) ^ 1;
               if (alive) alive = mbar_wait(bars.kempty(s), par, ctl, 12);
@@ -874,7 +874,7 @@ static int* take_unit_counter(const Ctx& c) {
   return static_cast<int*>(p);
 }
 
-template <int D, bool kCarry>
+template <int D, bool kCarry, bool kLog>
 static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
   using Cf = Cfg<D>;
   const Problem& p = a.p;
@@ -900,12 +900,12 @@ static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* l
   P.pairs_per_shard = (P.tiles_per_shard + 1) / 2;
   P.num_units = p.B * p.H * p.N * P.pairs_per_shard;
   P.scale_log2 = (float)(1.4426950408889634 / sqrt((double)p.D));
-  static std::atomic<bool> attr_set[256][2];  // idempotent attribute; atomic so threads may race
-  if (!attr_set[c.device][kCarry]) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, kCarry>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static std::atomic<bool> attr_set[256];  // idempotent attribute; atomic so threads may race
+  if (!attr_set[c.device]) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, kCarry, kLog>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Cf::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set[c.device][kCarry] = true;
+    attr_set[c.device] = true;
   }
   const int per_head = p.N * P.pairs_per_shard;
   const int num_super = (P.num_units / per_head) * ((per_head + 1) / 2);  // balanced unit pairs
@@ -919,7 +919,7 @@ static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* l
     P.group_heads = (int)std::max(1LL, std::min((long long)p.B * p.H, (48LL << 20) / kv));
   }
   const int grid = std::min(c.num_sms, P.unit_counter ? P.num_units : num_super);
-  fwd_bf16_kernel<D, kCarry><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, P);
+  fwd_bf16_kernel<D, kCarry, kLog><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, P);
   *launches += 1;
   cudaError_t e = cudaGetLastError();
   if (P.unit_counter) {
@@ -929,12 +929,20 @@ static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* l
   return e;
 }
 
+template <int D>
+static cudaError_t launch_fwd_bf16_dd(const FwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
+  // separate kernels with and without the ring-step carry and the visit log, so
+  // that the plain forward carries no code of either
+  const bool carry = a.o_carry != nullptr, log = a.vlog != nullptr;
+  if (carry) return log ? launch_fwd_bf16_d<D, true, true>(a, c, launches, why)
+                        : launch_fwd_bf16_d<D, true, false>(a, c, launches, why);
+  return log ? launch_fwd_bf16_d<D, false, true>(a, c, launches, why)
+             : launch_fwd_bf16_d<D, false, false>(a, c, launches, why);
+}
+
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const Ctx& c, uint64_t* launches, const char** why) {
-  const bool carry = a.o_carry != nullptr;
-  if (a.p.D == 64) return carry ? launch_fwd_bf16_d<64, true>(a, c, launches, why)
-                                : launch_fwd_bf16_d<64, false>(a, c, launches, why);
-  if (a.p.D == 128) return carry ? launch_fwd_bf16_d<128, true>(a, c, launches, why)
-                                 : launch_fwd_bf16_d<128, false>(a, c, launches, why);
+  if (a.p.D == 64) return launch_fwd_bf16_dd<64>(a, c, launches, why);
+  if (a.p.D == 128) return launch_fwd_bf16_dd<128>(a, c, launches, why);
   *why = "bf16 head_dim must be 64 or 128";
   return cudaSuccess;
 }
