@@ -446,6 +446,8 @@ def gpu_arm(args, peaks, peaks_src):
                          "frac_sustained": round(ftf / peak_s, 4), "peak_source": peaks_src,
                          "flops_per_launch": ffl,
                          "traffic": profile_traffic("ffn_7b", source_sha("ffn_sm103.cu", "sm103.cuh"))}}
+        # the ring across devices, all ranks' steps on this one GPU (device work of the ring-step kernels)
+        extra["ring_local_s65536"] = time_ring_local(ops, torch, WORKLOADS[5], max(2, args.steps // 2), dev, peak)
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
@@ -503,6 +505,49 @@ def decode_arm(args, peaks, peaks_src):
                       "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                                    "frac": round(gbs / hbm, 4), "peak_source": peaks_src,
                                    "algorithmic_bytes": dbytes}}), flush=True)
+
+
+def time_ring_local(ops, torch, w, iters, dev, peak):
+    """The fwd+bwd workload as a ring of N = w.num_shards ranks run one after another on
+    this GPU (ring.ring_forward_local / ring_backward_local): every ring-step kernel
+    launch of every rank, contiguous and striped blocks.  This is the device work a
+    rank does summed over the ring (no transfers), not the step time of a ring of
+    N GPUs; the FLOPs are the workload's."""
+    from long_context_exact_ra_gb300 import ring
+    x = make_inputs(w, with_dout=True)
+    q, k, v, do = (to_dev(getattr(x, n), torch, dev) for n in ("q", "k", "v", "dout"))
+    del x
+    B, S, H, D = q.shape
+    fl_f = F.fwd_flops_nominal(B, S, H, D, True)
+    fl_b = F.bwd_flops_nominal(B, S, H, D, True)
+    res = {"workload": f"{w.name}, as a ring of {w.num_shards} ranks on one GPU", "ranks": w.num_shards}
+    st = torch.cuda.current_stream()
+    for layout in ring.LAYOUTS:
+        n0 = ops.kernel_launches()
+        out, lse = ring.ring_forward_local(q, k, v, None, 1, w.num_shards, layout)  # warm-up
+        ring.ring_backward_local(q, k, v, out, lse, do, None, 1, w.num_shards, layout)
+        launches = ops.kernel_launches() - n0
+        ops.sync_check()
+        tf, tb = [], []
+        for _ in range(iters):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(st)
+            out, lse = ring.ring_forward_local(q, k, v, None, 1, w.num_shards, layout)
+            e[1].record(st)
+            ring.ring_backward_local(q, k, v, out, lse, do, None, 1, w.num_shards, layout)
+            e[2].record(st)
+            torch.cuda.synchronize()
+            tf.append(e[0].elapsed_time(e[1]))
+            tb.append(e[1].elapsed_time(e[2]))
+        ops.sync_check()
+        mf, mb = statistics.mean(tf), statistics.mean(tb)
+        res[layout] = {"fwd_ms": round(mf, 3), "bwd_ms": round(mb, 3),
+                       "fwd_tflops": round(fl_f / (mf * 1e-3) / 1e12, 1), "bwd_tflops": round(fl_b / (mb * 1e-3) / 1e12, 1),
+                       "fwd_frac": round(fl_f / (mf * 1e-3) / 1e12 / peak, 4),
+                       "bwd_frac": round(fl_b / (mb * 1e-3) / 1e12 / peak, 4),
+                       "launches_per_fwd_bwd": launches,
+                       "note": "timed region includes the carries' allocation and the host-side block shuffles"}
+    return res
 
 
 def time_ffn(ops, torch, wf, iters, warmup, dev):

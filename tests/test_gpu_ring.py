@@ -160,3 +160,34 @@ def test_two_ranks_on_one_gpu_host_staged(layout):
     check_lse(ring.unshard_lse(T(2), layout).numpy().astype(np.float64), ref_l, "bf16")
     for i, name, r in zip((3, 4, 5), ("dq", "dk", "dv"), oracle.ref_bwd(*f, seg, 1)):
         check_grad(ring.unshard(T(i), layout).numpy().astype(np.float64), r, name)
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+def test_ring_of_eight_at_s16384_sampled_rows(layout):
+    """A ring of 8 ranks over B1 S16384 H4 D128 (causal), forward and backward,
+    against the float64 oracle on sampled rows: 512 forward rows (shard and tile
+    edges forced), and dQ, dK, dV on 256 query and 256 key rows of one head with
+    that head's full lse and Delta."""
+    w = Workload("ring s16384", 1, 16384, 4, 128, "bf16", 1, 8, 2048, 2048, backward=True, seed=4242)
+    x = make_inputs(w, with_dout=True)
+    q, k, v, do = (to_dev(getattr(x, n), "bf16") for n in ("q", "k", "v", "dout"))
+    out, lse = ring.ring_forward_local(q, k, v, None, 1, 8, layout)
+    dq, dk, dv = ring.ring_backward_local(q, k, v, out, lse, do, None, 1, 8, layout)
+    ops.sync_check()
+    from long_context_exact_ra_gb300.inputs import bf16_bits_to_f32, sample_rows
+    rows = sample_rows(w.seed, w, 512)
+    qf, kf, vf = (bf16_bits_to_f32(getattr(x, n)) for n in ("q", "k", "v"))
+    ref_o, ref_l = oracle.ref_fwd_rows(qf, kf, vf, rows, None, 1)
+    ib, ih, ii = (torch.from_numpy(rows[:, c]).cuda() for c in range(3))
+    check_out(host_f64(out[ib, ii, ih]), ref_o, "bf16")
+    check_lse(lse[ib, ih, ii].cpu().numpy().astype(np.float64), ref_l, "bf16")
+    g = np.random.Generator(np.random.PCG64(17))
+    h = int(g.integers(w.heads))
+    qr = np.unique(np.concatenate([[0, 1, w.seq - 1], g.integers(w.seq, size=253)]))
+    kr = np.unique(np.concatenate([[0, 2047, 2048, w.seq - 1], g.integers(w.seq, size=252)]))
+    Q, K, V, dO = (as_f64(getattr(x, n)[0, :, h], "bf16") for n in ("q", "k", "v", "dout"))
+    rq, rk, rv = oracle.ref_bwd_head_blocked(Q, K, V, dO, None, 1, qr, kr, block=2048)
+    iq, ik = torch.from_numpy(qr).cuda(), torch.from_numpy(kr).cuda()
+    check_grad(host_f64(dq[0, iq, h]), rq, "dq rows")
+    check_grad(host_f64(dk[0, ik, h]), rk, "dk rows")
+    check_grad(host_f64(dv[0, ik, h]), rv, "dv rows")
