@@ -80,6 +80,17 @@ def unshard_lse(blocks, layout: str) -> torch.Tensor:
     return unshard([b.transpose(1, 2) for b in blocks], layout).transpose(1, 2).contiguous()
 
 
+def check_layout(layout: str, causal_block_size: int) -> None:
+    """Reject what the ring-step calls do not support, before any block moves (a rank
+    that failed inside the ring would leave its neighbours waiting on a transfer)."""
+    if layout not in LAYOUTS:
+        raise ValueError(f"unknown layout {layout!r} (one of {LAYOUTS})")
+    if causal_block_size < 0:
+        raise ValueError("causal_block_size must be >= 0")
+    if layout == "striped" and causal_block_size > 1:
+        raise ValueError("striped blocks support causal_block_size 0 or 1")
+
+
 def block_sees_nothing(layout: str, c: int, q0: int, k0: int, L: int) -> bool:
     """True when no key of the k/v block is visible to any query of the block (the
     step can be skipped; the kernels would skip every tile of it anyway)."""
@@ -205,6 +216,7 @@ def ring_forward(q, k, v, segment_ids=None, causal_block_size=0, layout="contigu
     """Forward of this rank's block: q, k, v [B, L, H, D] and segment_ids [B, L] are
     the block the rank holds under `layout`.  Returns (out [B, L, H, D] like q,
     lse [B, H, L] float32) for the rank's queries."""
+    check_layout(layout, causal_block_size)
     tr = transport or ProcessGroupTransport()
     kern = kernels or CudaRingKernels()
     rank, world = tr.rank, tr.world
@@ -226,6 +238,7 @@ def ring_backward(q, k, v, out, lse, dout, segment_ids=None, causal_block_size=0
     travel around the ring again, each with its float32 dK, dV; the next block is
     posted before the current one's gradients are computed, and the gradients
     follow once they are.  Returns (dq, dk, dv) for the rank's own block."""
+    check_layout(layout, causal_block_size)
     tr = transport or ProcessGroupTransport()
     kern = kernels or CudaRingKernels()
     rank, world = tr.rank, tr.world
@@ -254,6 +267,7 @@ def ring_forward_local(q, k, v, segment_ids=None, causal_block_size=0, world=2, 
     the sequence is cut into blocks under `layout`, every rank's step runs in
     turn, and the blocks move to the next rank between steps.  Returns the full
     (out, lse) in sequence order."""
+    check_layout(layout, causal_block_size)
     kern = kernels or CudaRingKernels()
     L = q.shape[1] // world
     qs = [shard(q, layout, world, r) for r in range(world)]
@@ -271,6 +285,7 @@ def ring_forward_local(q, k, v, segment_ids=None, causal_block_size=0, world=2, 
 def ring_backward_local(q, k, v, out, lse, dout, segment_ids=None, causal_block_size=0, world=2,
                         layout="contiguous", kernels=None):
     """Backward of `ring_forward_local` (full tensors in, full dq, dk, dv out)."""
+    check_layout(layout, causal_block_size)
     kern = kernels or CudaRingKernels()
     L = q.shape[1] // world
     sh = lambda x, r: shard(x, layout, world, r)  # noqa: E731

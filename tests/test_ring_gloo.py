@@ -103,3 +103,14 @@ def test_layouts_round_trip_and_positions():
             p0, st = ring.block_positions(layout, r, 4, 3)
             pos = p0 + st * torch.arange(3)
             assert torch.equal(blocks[r][0, :, 0] // 3, pos)  # element value // 3 = its position
+
+
+def test_unsupported_layouts_are_rejected_before_any_transfer():
+    from long_context_exact_ra_gb300 import ring
+    x = torch.zeros(1, 8, 1, 4)
+    with pytest.raises(ValueError):
+        ring.ring_forward_local(x, x, x, None, 3, 2, "striped")
+    with pytest.raises(ValueError):
+        ring.ring_backward(x, x, x, x, x, x, None, 2, "striped", transport=object(), kernels=object())
+    with pytest.raises(ValueError):
+        ring.ring_forward(x, x, x, None, 1, "diagonal", transport=object(), kernels=object())
