@@ -432,6 +432,7 @@ def gpu_arm(args, peaks, peaks_src):
                 tfv = flv / (msm * 1e-3) / 1e12
                 line["roofline"].update({"visible_flops_per_launch": flv, "achieved_visible": round(tfv, 1),
                                          "frac_visible": round(tfv / peak, 4), "frac": round(tfv / peak, 4),
+                                         "frac_sustained": round(tfv / peak_s, 4),
                                          "achieved": round(tfv, 1), "achieved_nominal": round(tfc, 1),
                                          "note": "achieved and frac count visible pairs only"})
             extra[f"fwd_cfg{cfg}"] = line

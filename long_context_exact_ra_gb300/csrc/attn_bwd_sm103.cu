@@ -797,9 +797,12 @@ static cudaError_t launch_bwd_main(const BwdArgs& a, const Ctx& c, uint64_t* lau
   P.dv_carry = a.dv_carry;
   P.vlog = a.vlog;
   P.vlog_cap = a.vlog_cap;
-  {  // heads whose Q, dO (bf16) and dQ accumulator (fp32), 8 * S * D bytes, fit in 48 MB of L2
+  {  // heads whose Q, dO (bf16) and dQ accumulator (fp32), 8 * S * D bytes, fit in
+     // 48 MB of L2 together, or in 128 MB when one head's take 16 MB or less (the
+     // forward's rule: balance for short heads, no DRAM re-reads for long ones)
     const long long per = 8LL * p.S * p.D;
-    P.group_heads = (int)std::max(1LL, std::min((long long)p.B * p.H, (48LL << 20) / per));
+    const long long budget = per <= (16LL << 20) ? (128LL << 20) : (48LL << 20);
+    P.group_heads = (int)std::max(1LL, std::min((long long)p.B * p.H, budget / per));
   }
   static std::atomic<bool> attr_set[256];  // idempotent attribute; atomic so threads may race
   if (!attr_set[c.device]) {

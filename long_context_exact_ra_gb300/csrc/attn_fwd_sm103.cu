@@ -914,9 +914,13 @@ static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* l
   // capture the static pairs are used instead (same results: each unit is computed
   // whole by one CTA either way).
   P.unit_counter = take_unit_counter(c);
-  {  // heads whose K and V (2 * S * D bf16 each) fit in 48 MB of L2 together
+  {  // heads whose K and V (2 * S * D bf16 each) fit in 48 MB of L2 together, or in
+     // 128 MB when one head's take 16 MB or less: short heads have few units each,
+     // and a small last group cannot balance its longest units, so the SMs idle at
+     // the end of the launch; long heads past 48 MB only re-read K and V from DRAM
     const long long kv = 2LL * p.S * p.D * 2;
-    P.group_heads = (int)std::max(1LL, std::min((long long)p.B * p.H, (48LL << 20) / kv));
+    const long long budget = kv <= (16LL << 20) ? (128LL << 20) : (48LL << 20);
+    P.group_heads = (int)std::max(1LL, std::min((long long)p.B * p.H, budget / kv));
   }
   const int grid = std::min(c.num_sms, P.unit_counter ? P.num_units : num_super);
   fwd_bf16_kernel<D, kCarry, kLog><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, P);
