@@ -457,26 +457,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t mdQ = sdesc_sw128(sbase + C::OFF_Q, 16384, 1024);  // Q stage 0, MN-major
       const uint64_t mdO = sdesc_sw128(sbase + C::OFF_DO, 16384, 1024); // dO stage 0, MN-major
       const uint64_t mdS = sdesc_sw128(sbase + C::OFF_DS, 16384, 1024); // dS^T, MN-major
-      while (alive) {
+      // This thread needs only each record's kind.  It reads the next record while
+      // the P/dS warpgroups work on the current pair (and frees its slot at once),
+      // so that the next pair's MMAs follow the current pair's without a gap.
+      auto fetch_kind = [&](int& kind) -> bool {
         const int slot = rec_n % kNInfo;
-        if (!mbar_wait(bars.infofull(slot), (rec_n / kNInfo) & 1, ctl, 50)) break;
-        const BRec r = recs[slot];
-        if (r.kind == kRecStop) {
-          mbar_arrive(bars.infoempty(slot));
-          break;
-        }
+        if (!mbar_wait(bars.infofull(slot), (rec_n / kNInfo) & 1, ctl, 50)) return false;
+        kind = recs[slot].kind;
+        mbar_arrive(bars.infoempty(slot));
+        ++rec_n;
+        return true;
+      };
+      int kind = kRecStop;
+      alive = fetch_kind(kind);
+      while (alive) {
+        if (kind == kRecStop) break;
         if (!in_unit) {  // first record of a unit: its K/V tiles must be resident
           if (!mbar_wait(bars.kvfull(), unit_n & 1, ctl, 51)) break;
           in_unit = true;
           unit_pairs = 0;
         }
-        if (r.kind == kRecUnitEnd) {
+        if (kind == kRecUnitEnd) {
           mma_commit(bars.accdone());
           mma_commit(bars.kvempty());
-          mbar_arrive(bars.infoempty(slot));
-          ++rec_n;
           ++unit_n;
           in_unit = false;
+          alive = fetch_kind(kind);
           continue;
         }
         const bool first = unit_pairs == 0;
@@ -498,6 +504,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tA, sdesc_add(kdK, off), sdesc_add(kdQ, s * C::TB + off), idSP, kk > 0);
         }
         mma_commit(bars.spfull());
+        // the record after this pair (a pair or the unit's end: the producer
+        // publishes either without waiting for this pair)
+        int next_kind = kRecStop;
+        if (!fetch_kind(next_kind)) break;
         // wait for P^T, dS^T (TMEM) and dS^T (smem)
         if (!mbar_wait(bars.pready(), pready_ph, ctl, 54)) break;
         pready_ph ^= 1;
@@ -537,8 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++dq_n;
         ++pair_n;
         ++unit_pairs;
-        mbar_arrive(bars.infoempty(slot));
-        ++rec_n;
+        kind = next_kind;
       }
       // drain every MMA before TMEM is freed
       mma_commit(bars.kvempty());
