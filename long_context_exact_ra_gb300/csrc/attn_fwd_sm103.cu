@@ -21,7 +21,8 @@
 //   warp 9     MMA issuer: S_w = Q_w K^T (SS, fp32 in TMEM), then
 //              O_w += P_w V with P_w read from TMEM (TS), ping-ponging the two
 //              Q tiles so the tensor pipe runs one tile's MMAs while the other
-//              tile's softmax runs.
+//              tile's softmax runs.  At D = 64 warps 9 and 10 each issue one Q
+//              tile's MMAs instead (Cfg::ISSUERS).
 // Tensor memory (512 columns): S0 | S1 | O0 | O1.  P_w is written as packed
 // bf16 pairs over the first 64 columns of S_w.
 // The running max is only moved (and O, l rescaled) when a row's tile max
@@ -43,7 +44,6 @@ namespace {
 constexpr int kBM = 128;  // rows per Q tile
 constexpr int kBN = 128;  // keys per KV tile
 constexpr int kNInfo = 8; // schedule-record ring depth
-constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -65,6 +65,12 @@ struct __align__(16) Rec {
 
 template <int D>
 struct Cfg {
+  // MMA issuers: at D = 128 one thread issues both Q tiles' MMAs in the order
+  // PV0, S0, PV1, S1, which keeps one tile's MMAs under the other tile's softmax.
+  // At D = 64 the MMAs are short, and one issuer per Q tile (warps 9 and 10) lets
+  // each tile's chain run without waiting on the other's softmax.
+  static constexpr int ISSUERS = (D == 64) ? 2 : 1;
+  static constexpr int THREADS = 32 * (9 + ISSUERS);     // softmax 0-7, producer 8, MMA 9 (and 10)
   static constexpr int KST = (D == 64) ? 4 : 2;          // K/V ring stages
   static constexpr uint32_t QT = kBM * D * 2;            // bytes of one Q tile
   static constexpr uint32_t KVT = kBN * D * 2;           // bytes of one K or V tile
@@ -157,7 +163,7 @@ __device__ __forceinline__ int ticket_unit(const FwdParams& P, int t) {
 }
 
 template <int D, bool kCarry, bool kLog>
-__global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-partitions -> <= 168 registers
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some SM sub-partitions -> <= 168 registers
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const FwdParams P) {
   using C = Cfg<D>;
@@ -174,16 +180,16 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bars.qfull(), 1);
-    mbar_init(bars.qempty(), 1);
+    mbar_init(bars.qempty(), C::ISSUERS);  // one commit per MMA issuer
     for (int s = 0; s < C::KST; ++s) {
       mbar_init(bars.kfull(s), 1);
-      mbar_init(bars.kempty(s), 1);
+      mbar_init(bars.kempty(s), C::ISSUERS);
       mbar_init(bars.vfull(s), 1);
-      mbar_init(bars.vempty(s), 1);
+      mbar_init(bars.vempty(s), C::ISSUERS);
     }
     for (int i = 0; i < kNInfo; ++i) {
       mbar_init(bars.infofull(i), 1);
-      mbar_init(bars.infoempty(i), 1 + 8);  // MMA thread + one lane per softmax warp
+      mbar_init(bars.infoempty(i), C::ISSUERS + 8);  // MMA threads + one lane per softmax warp
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(bars.sfull(w), 1);
@@ -445,10 +451,11 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
       }
       if (q_loads > 0) mbar_drain(bars.qfull(), (q_loads - 1) & 1, ctl, 16);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || (C::ISSUERS == 2 && warp == kMmaWarp + 1)) {
     // ------------------------------------------------------------------
-    // MMA issuer (lane 0)
+    // MMA issuer(s) (lane 0): both Q tiles, or (two issuers) the warp's own
     // ------------------------------------------------------------------
+    const int mw = warp - kMmaWarp;
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 0, 1);
@@ -470,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
       auto issue_S = [&](const MRec& r, int stage) -> bool {
         if (!mbar_wait(bars.kfull(stage), (tile_n / C::KST) & 1, ctl, 21)) return false;
         tc_fence_after();
-        for (int w = 0; w < 2; ++w) {
+        for (int w = C::ISSUERS == 2 ? mw : 0; C::ISSUERS == 2 ? w == mw : w < 2; ++w) {
           if (r.flags & (w == 0 ? kSkip0 : kSkip1)) continue;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -516,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
           if (!mbar_wait(bars.vfull(stage), (tile_n / C::KST) & 1, ctl, 23)) { alive = false; break; }
           const int nstage = (tile_n + 1) % C::KST;
           bool nxt_k_ready = false;
-          for (int w = 0; w < 2 && alive; ++w) {
+          for (int w = C::ISSUERS == 2 ? mw : 0; (C::ISSUERS == 2 ? w == mw : w < 2) && alive; ++w) {
             if (!(rec.flags & (w == 0 ? kSkip0 : kSkip1))) {
               if (first[w]) {
                 if (!mbar_wait(bars.ofree(w), ofree_ph[w], ctl, 24)) { alive = false; break; }
@@ -553,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
           ++tile_n;
           stage = nstage;
           if (nxt.kind != kRecTile) {  // unit end
-            for (int w = 0; w < 2; ++w)
+            for (int w = C::ISSUERS == 2 ? mw : 0; C::ISSUERS == 2 ? w == mw : w < 2; ++w)
               if (any_pv[w]) mma_commit(bars.odone(w));
             mma_commit(bars.qempty());
             release(nxt_i);
@@ -573,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)  // 10 warps: 3 on some SM sub-pa
       mbar_drain(bars.qempty(), (unit_n & 1), ctl, 27);
     }
     __syncwarp();
-  } else {
+  } else if (C::ISSUERS == 1 || warp < 8) {
     // ------------------------------------------------------------------
     // Softmax warpgroups: w = Q tile, one row per thread
     // ------------------------------------------------------------------
@@ -923,7 +930,7 @@ static cudaError_t launch_fwd_bf16_d(const FwdArgs& a, const Ctx& c, uint64_t* l
     P.group_heads = (int)std::max(1LL, std::min((long long)p.B * p.H, budget / kv));
   }
   const int grid = std::min(c.num_sms, P.unit_counter ? P.num_units : num_super);
-  fwd_bf16_kernel<D, kCarry, kLog><<<grid, kThreads, Cf::SMEM, c.stream>>>(mq, mk, mv, P);
+  fwd_bf16_kernel<D, kCarry, kLog><<<grid, Cf::THREADS, Cf::SMEM, c.stream>>>(mq, mk, mv, P);
   *launches += 1;
   cudaError_t e = cudaGetLastError();
   if (P.unit_counter) {
