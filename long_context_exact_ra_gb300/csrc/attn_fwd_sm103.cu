@@ -193,9 +193,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(bars.sfull(w), 1);
-      mbar_init(bars.pready(w), 128);
+      mbar_init(bars.pready(w), 4);  // one arrival per softmax warp
       mbar_init(bars.odone(w), 1);
-      mbar_init(bars.ofree(w), 128);
+      mbar_init(bars.ofree(w), 4);
     }
     fence_mbar_init();
   }
@@ -712,7 +712,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bars.pready(w));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.pready(w));
         ++processed;
       } else if (r.kind == kRecUnitEnd) {
         if (processed > 0) {
@@ -789,7 +790,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
             }
           }
           tc_fence_before();
-          mbar_arrive(bars.ofree(w));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.ofree(w));
         }
         m_use = -INFINITY;
         l = 0.f;
