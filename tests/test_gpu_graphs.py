@@ -120,7 +120,8 @@ def _fwd_static_and_dynamic(q, k, v, seg, c, N):
 
 @pytest.mark.parametrize("B,S,H,D,N,c,docs", [
     (3, 1536, 5, 64, 3, 1, True),      # packed documents, one head group, units of uneven cost
-    (2, 32768, 2, 128, 4, 1, False),   # 16 MB of K/V per head: groups of 3 heads, the last one short
+    (1, 40960, 3, 128, 4, 1, False),   # 20 MB of K/V per head (48 MB groups): 2 heads, then a short group of 1
+    (2, 8192, 20, 128, 4, 1, False),   # 4 MB of K/V per head (128 MB groups): 32 heads, then a short group of 8
     (1, 1000, 3, 128, 2, 0, False),    # ragged shards, non-causal
 ])
 def test_forward_unit_schedule_does_not_change_results(B, S, H, D, N, c, docs):
