@@ -455,6 +455,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
     // ------------------------------------------------------------------
     // MMA issuer(s) (lane 0): both Q tiles, or (two issuers) the warp's own
     // ------------------------------------------------------------------
+    // Q tiles this thread issues: w = 0, 1 with one issuer; w = mw with two.  The
+    // loop bounds below fold to exactly those two forms at compile time (written
+    // any other way, the generated code of both instances ran slower).
     const int mw = warp - kMmaWarp;
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
@@ -580,7 +583,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
       mbar_drain(bars.qempty(), (unit_n & 1), ctl, 27);
     }
     __syncwarp();
-  } else if (C::ISSUERS == 1 || warp < 8) {
+  } else if (C::ISSUERS == 1 || warp < 8) {  // with one issuer, every remaining warp (0-7)
     // ------------------------------------------------------------------
     // Softmax warpgroups: w = Q tile, one row per thread
     // ------------------------------------------------------------------
