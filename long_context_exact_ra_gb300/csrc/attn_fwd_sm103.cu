@@ -83,7 +83,13 @@ struct Cfg {
   //           infofull[8], infoempty[8], sfull[2], pready[2], odone[2], ofree[2]
   static constexpr int NBAR = 2 + 4 * KST + 2 * kNInfo + 8;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
+  // Segment-id (min, max) of every key tile (b, shard, tile), built at kernel
+  // start when segment ids are given and the tiles fit (else the producer reads
+  // each tile's ids itself).  D = 64 only, the head size of the packed-document
+  // workloads: at D = 128 the extra code cost the unsegmented forward ~0.5 %.
+  static constexpr int SUMCAP = (D == 64) ? 4096 : 0;
+  static constexpr uint32_t OFF_SUM = OFF_MISC + 64;
+  static constexpr uint32_t SMEM = OFF_SUM + SUMCAP * 8 + 1024;  // + alignment slack
   static constexpr uint32_t TCOL_O = 256;                 // O0 at 256, O1 at 256 + D
 };
 
@@ -203,6 +209,50 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  // Key segment summary: warp-per-tile, 4 ids per lane, 8 tiles in flight.
+  const int nsum = (C::SUMCAP > 0 && P.p.seg) ? P.p.B * P.p.N * P.tiles_per_shard : 0;
+  const bool use_sum = C::SUMCAP > 0 && nsum > 0 && nsum <= C::SUMCAP;
+  int2* ksum = reinterpret_cast<int2*>(sm + C::OFF_SUM);
+  if constexpr (C::SUMCAP > 0) if (use_sum) {
+    const int* kids = kCarry ? P.kseg : P.p.seg;
+    const int nwarps = C::THREADS / 32;
+    for (int e0 = warp * 8; e0 < nsum; e0 += nwarps * 8) {
+      int mn[8], mx[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        mn[u] = INT_MAX;
+        mx[u] = INT_MIN;
+        const int e = e0 + u;
+        if (e < nsum) {
+          const int t = e % P.tiles_per_shard, bk = e / P.tiles_per_shard;
+          const int k = bk % P.p.N, bb = bk / P.p.N;
+          const int ka = k * P.p.Ssh + t * kBN;
+          const int n = min(kBN, (k + 1) * P.p.Ssh - ka);
+          const int* sp = kids + (size_t)bb * P.p.S + ka;
+          if (n == kBN && ((reinterpret_cast<uintptr_t>(sp) & 15u) == 0)) {
+            const int4 v4 = __ldg(reinterpret_cast<const int4*>(sp) + lane);
+            mn[u] = min(min(v4.x, v4.y), min(v4.z, v4.w));
+            mx[u] = max(max(v4.x, v4.y), max(v4.z, v4.w));
+          } else {
+            for (int x = lane; x < n; x += 32) {
+              const int v = __ldg(sp + x);
+              mn[u] = min(mn[u], v);
+              mx[u] = max(mx[u], v);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          mn[u] = min(mn[u], __shfl_xor_sync(0xffffffffu, mn[u], o));
+          mx[u] = max(mx[u], __shfl_xor_sync(0xffffffffu, mx[u], o));
+        }
+        if (lane == 0 && e0 + u < nsum) ksum[e0 + u] = make_int2(mn[u], mx[u]);
+      }
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -276,7 +326,19 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
       const int qv1 = max(0, min(kBM, shard0 + pb.Ssh - (q0 + kBM)));
       // segment range of each Q tile
       int qmin[2] = {0, 0}, qmax[2] = {0, 0};
-      if (pb.seg) {
+      if (pb.seg && use_sum && !kCarry) {
+        for (int w = 0; w < 2; ++w) {
+          const int tq = pr * 2 + w;
+          const int nv = w == 0 ? qv0 : qv1;
+          qmin[w] = INT_MAX;
+          qmax[w] = INT_MIN;
+          if (nv > 0 && tq < P.tiles_per_shard) {
+            const int2 mm = ksum[((size_t)b * pb.N + j) * P.tiles_per_shard + tq];
+            qmin[w] = mm.x;
+            qmax[w] = mm.y;
+          }
+        }
+      } else if (pb.seg) {
         for (int w = 0; w < 2; ++w) {
           const int nv = w == 0 ? qv0 : qv1;
           int mn = INT_MAX, mx = INT_MIN;
@@ -322,7 +384,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
             const int kb = min(kend, ka + kBN);
             bool needed = !(c > 0 && floordiv_pos(qlast + qo, c) < floordiv_pos(ka + ko, c));
             int mn = INT_MAX, mx = INT_MIN;
-            if (needed) {
+            if (needed && use_sum) {
+              const int2 mm = ksum[((size_t)b * pb.N + ks) * P.tiles_per_shard + my_t];
+              mn = mm.x;
+              mx = mm.y;
+            } else if (needed) {
               const int* sp = (kCarry ? P.kseg : pb.seg) + (size_t)b * pb.S + ka;
               if (kb - ka == kBN && ((reinterpret_cast<uintptr_t>(sp) & 15u) == 0)) {
 #pragma unroll 8
