@@ -592,6 +592,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
           if (!mbar_wait(bars.vfull(stage), (tile_n / C::KST) & 1, ctl, 23)) { alive = false; break; }
           const int nstage = (tile_n + 1) % C::KST;
           bool nxt_k_ready = false;
+          // The unit's last tile: every S (the only MMAs that read Q) is already
+          // issued, so at D = 64 (short packed-document units) Q's buffer is
+          // released before the last PVs and the next unit's Q tiles load under them.
+          if (C::ISSUERS == 2 && nxt.kind != kRecTile) mma_commit(bars.qempty());
           for (int w = C::ISSUERS == 2 ? mw : 0; (C::ISSUERS == 2 ? w == mw : w < 2) && alive; ++w) {
             if (!(rec.flags & (w == 0 ? kSkip0 : kSkip1))) {
               if (first[w]) {
@@ -631,7 +635,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
           if (nxt.kind != kRecTile) {  // unit end
             for (int w = C::ISSUERS == 2 ? mw : 0; C::ISSUERS == 2 ? w == mw : w < 2; ++w)
               if (any_pv[w]) mma_commit(bars.odone(w));
-            mma_commit(bars.qempty());
+            if (C::ISSUERS == 1) mma_commit(bars.qempty());
             release(nxt_i);
             rec_i = nxt_i + 1;
             ++unit_n;
