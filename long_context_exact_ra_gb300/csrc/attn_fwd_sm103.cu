@@ -24,7 +24,9 @@
 //              tile's softmax runs.  At D = 64 warps 9 and 10 each issue one Q
 //              tile's MMAs instead (Cfg::ISSUERS).
 // Tensor memory (512 columns): S0 | S1 | O0 | O1.  P_w is written as packed
-// bf16 pairs over the first 64 columns of S_w.
+// bf16 pairs over the first 64 columns of S_w at D = 128; at D = 64 it has
+// columns of its own (S0 | S1 | O0 | O1 | P0 | P1), so S_w(t + 1) can be issued
+// once the softmax has read S_w(t), ahead of PV_w(t).
 // The running max is only moved (and O, l rescaled) when a row's tile max
 // exceeds it by more than 2^8; in exact arithmetic the result is unchanged
 // (numerator and denominator carry the same factor), and the exponentials
@@ -81,7 +83,7 @@ struct Cfg {
   static constexpr uint32_t OFF_BAR = OFF_REC + kNInfo * sizeof(Rec);
   // barriers: qfull, qempty, kfull[KST], kempty[KST], vfull[KST], vempty[KST],
   //           infofull[8], infoempty[8], sfull[2], pready[2], odone[2], ofree[2]
-  static constexpr int NBAR = 2 + 4 * KST + 2 * kNInfo + 8;
+  static constexpr int NBAR = 2 + 4 * KST + 2 * kNInfo + 8 + ((D == 64) ? 4 : 0);  // + sread[2], pfree[2]
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   // Segment-id (min, max) of every key tile (b, shard, tile), built at kernel
   // start when segment ids are given and the tiles fit (else the producer reads
@@ -91,6 +93,10 @@ struct Cfg {
   static constexpr uint32_t OFF_SUM = OFF_MISC + 64;
   static constexpr uint32_t SMEM = OFF_SUM + SUMCAP * 8 + 1024;  // + alignment slack
   static constexpr uint32_t TCOL_O = 256;                 // O0 at 256, O1 at 256 + D
+  // D = 64: P_w in columns of its own (384 + 64 w), so S_w(t + 1) can be written
+  // as soon as the softmax has read S_w(t), ahead of PV_w(t).
+  static constexpr bool PSEP = (D == 64);
+  static constexpr uint32_t TCOL_P = 256 + 2 * D;
 };
 
 struct Bars {
@@ -108,6 +114,8 @@ struct Bars {
   __device__ uint32_t pready(int w) const { return base + 16 + 8 * (4 * kst + 2 * kNInfo + 2 + w); }
   __device__ uint32_t odone(int w) const { return base + 16 + 8 * (4 * kst + 2 * kNInfo + 4 + w); }
   __device__ uint32_t ofree(int w) const { return base + 16 + 8 * (4 * kst + 2 * kNInfo + 6 + w); }
+  __device__ uint32_t sread(int w) const { return base + 16 + 8 * (4 * kst + 2 * kNInfo + 8 + w); }
+  __device__ uint32_t pfree(int w) const { return base + 16 + 8 * (4 * kst + 2 * kNInfo + 10 + w); }
 };
 
 struct FwdParams {
@@ -202,6 +210,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
       mbar_init(bars.pready(w), 4);  // one arrival per softmax warp
       mbar_init(bars.odone(w), 1);
       mbar_init(bars.ofree(w), 4);
+      if constexpr (C::PSEP) {
+        mbar_init(bars.sread(w), 4);  // one arrival per softmax warp: S_w read into registers
+        mbar_init(bars.pfree(w), 1);  // MMA commit after PV_w: P_w and O_w may be written
+      }
     }
     fence_mbar_init();
   }
@@ -531,6 +543,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
       int tile_n = 0, unit_n = 0;
       uint32_t ofree_ph[2] = {1, 1}, pready_ph[2] = {0, 0};
       bool alive = true;
+      int s_n[2] = {0, 0};  // S issued per Q tile (PSEP: the softmax reads each once)
       // Shared-memory descriptors of every operand buffer, built once; each MMA
       // adds a compile-time byte offset.
       const uint64_t dQ0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
@@ -548,6 +561,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
         tc_fence_after();
         for (int w = C::ISSUERS == 2 ? mw : 0; C::ISSUERS == 2 ? w == mw : w < 2; ++w) {
           if (r.flags & (w == 0 ? kSkip0 : kSkip1)) continue;
+          if constexpr (C::PSEP) {
+            if (s_n[w] > 0 && !mbar_wait(bars.sread(w), (s_n[w] - 1) & 1, ctl, 28)) return false;
+            ++s_n[w];
+            tc_fence_after();
+          }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -596,6 +614,37 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
           // issued, so at D = 64 (short packed-document units) Q's buffer is
           // released before the last PVs and the next unit's Q tiles load under them.
           if (C::ISSUERS == 2 && nxt.kind != kRecTile) mma_commit(bars.qempty());
+          if constexpr (C::PSEP) {
+            const int w = mw;
+            if (nxt.kind == kRecTile && !(nxt.flags & (w == 0 ? kSkip0 : kSkip1))) {
+              if (!mbar_wait(bars.kfull(nstage), ((tile_n + 1) / C::KST) & 1, ctl, 26)) { alive = false; break; }
+              if (s_n[w] > 0 && !mbar_wait(bars.sread(w), (s_n[w] - 1) & 1, ctl, 28)) { alive = false; break; }
+              ++s_n[w];
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                mma_ss(tbase + w * 128, sdesc_add(dQ(w), off), sdesc_add(dK(nstage), off), idS, kk > 0);
+              }
+              mma_commit(bars.sfull(w));
+            }
+            if (!(rec.flags & (w == 0 ? kSkip0 : kSkip1))) {
+              if (first[w]) {
+                if (!mbar_wait(bars.ofree(w), ofree_ph[w], ctl, 24)) { alive = false; break; }
+                ofree_ph[w] ^= 1;
+              }
+              if (!mbar_wait(bars.pready(w), pready_ph[w], ctl, 25)) { alive = false; break; }
+              pready_ph[w] ^= 1;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < kBN / 16; ++kk)
+                mma_ts(tbase + C::TCOL_O + w * D, tbase + C::TCOL_P + w * 64 + kk * 8, sdesc_add(dV(stage), kk * 2048),
+                       idO, first[w] ? (kk > 0) : 1);
+              mma_commit(bars.pfree(w));
+              first[w] = false;
+              any_pv[w] = true;
+            }
+          } else
           for (int w = C::ISSUERS == 2 ? mw : 0; (C::ISSUERS == 2 ? w == mw : w < 2) && alive; ++w) {
             if (!(rec.flags & (w == 0 ? kSkip0 : kSkip1))) {
               if (first[w]) {
@@ -662,6 +711,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tbase + lane_base + w * 128;
     const uint32_t tO = tbase + lane_base + C::TCOL_O + w * D;
+    const uint32_t tP = C::PSEP ? tbase + lane_base + C::TCOL_P + w * 64 : tS;  // where P_w goes
+    int p_n = 0;  // P stores so far (PSEP: each waits for the previous PV_w)
     const float sl2 = P.scale_log2;
     float m_use = -INFINITY, l = 0.f;
     int processed = 0;
@@ -691,6 +742,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
         for (int cq = 0; cq < 4; ++cq) tmem_ld32(tS + cq * 32, sr + cq * 32);
 #pragma unroll
         for (int cq = 0; cq < 4; ++cq) tmem_ld_wait(sr + cq * 32);
+        if constexpr (C::PSEP) {  // S_w is in registers: its columns may take S_w(t + 1)
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.sread(w));
+        }
         if (r.flags & (w == 0 ? kMask0 : kMask1)) {
           // keys x < nvis of the tile pass the range and causal rules: the causal
           // block of key kstart + x must not exceed the row's block
@@ -757,6 +813,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
           m_use = m_tile;
         }
         const float mb = (m_use == -INFINITY) ? 0.f : m_use;
+        if constexpr (C::PSEP) {  // the previous PV_w has read P_w and written O_w
+          if (p_n > 0) {
+            alive = __all_sync(0xffffffffu, mbar_wait(bars.pfree(w), (p_n - 1) & 1, ctl, 33));
+            if (!alive) break;
+          }
+          ++p_n;
+          tc_fence_after();
+        }
         float rs[4] = {0.f, 0.f, 0.f, 0.f};  // two packed accumulators
         uint32_t pk[64];
 #pragma unroll
@@ -768,9 +832,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
           const int acc = (x & 1) * 2;
           add_f32x2(rs[acc], rs[acc + 1], rs[acc], rs[acc + 1], p0, p1);
           pk[x] = pack_bf16x2(p0, p1);
-          if (x == 31) tmem_st32(tS, pk);  // first half of P goes out while the rest is computed
+          if (x == 31) tmem_st32(tP, pk);  // first half of P goes out while the rest is computed
         }
-        tmem_st32(tS + 32, pk + 32);
+        tmem_st32(tP + 32, pk + 32);
         l = l * corr + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
         if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
