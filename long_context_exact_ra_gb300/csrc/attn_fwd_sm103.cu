@@ -10,14 +10,16 @@
 // §2 数值稳定的注意力计算); tiles with no visible element are skipped (§3,
 // below_or_on_diag), and segment ids mask across documents.
 //
-// How (one persistent CTA per SM, 10 warps):
+// How (one persistent CTA per SM, 10 warps; 11 at D = 64):
 //   warps 0-3  softmax warpgroup for Q tile 0 (TMEM lanes 0-127, one row per thread)
 //   warps 4-7  softmax warpgroup for Q tile 1
 //   warp 8     producer: takes query-tile-pair units (from a per-call counter,
 //              or a fixed schedule under stream capture), walks the ring
 //              schedule, classifies 32 key tiles at once (one per lane: skip /
-//              full / needs a mask), publishes a record per visible tile and
-//              TMA-loads K and V into a smem ring (128B swizzle)
+//              full / needs a mask; at D = 64 from a per-tile segment-id
+//              summary that all warps build in smem at kernel start), publishes
+//              a record per visible tile and TMA-loads K and V into a smem ring
+//              (128B swizzle)
 //   warp 9     MMA issuer: S_w = Q_w K^T (SS, fp32 in TMEM), then
 //              O_w += P_w V with P_w read from TMEM (TS), ping-ponging the two
 //              Q tiles so the tensor pipe runs one tile's MMAs while the other
