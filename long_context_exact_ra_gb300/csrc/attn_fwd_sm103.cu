@@ -606,7 +606,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)  // 10-11 warps: 3 on some
         bool any_pv[2] = {false, false};
         while (alive) {
           // rec: tile t (record rec_i); nxt: record t + 1 (a tile or the unit end).
-          // Order on the tensor pipe: PV0(t), S0(t+1), PV1(t), S1(t+1).
+          // Order on the tensor pipe: PV0(t), S0(t+1), PV1(t), S1(t+1) with one
+          // issuer; with P in columns of its own (PSEP), each issuer sends
+          // S_w(t+1) once its softmax has read S_w(t), then PV_w(t).
           const int nxt_i = rec_i + 1;
           if (!take_at(nxt, nxt_i)) { alive = false; break; }
           if (!mbar_wait(bars.vfull(stage), (tile_n / C::KST) & 1, ctl, 23)) { alive = false; break; }
