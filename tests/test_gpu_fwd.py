@@ -67,6 +67,7 @@ SMALL_BF16 = [
     (1024, 4, 1, 128, 256, 300, 0.5),     # packed documents + causal
     (1024, 4, 0, 64, 256, 200, 1.0),      # segments, non-causal
     (896, 7, 1, 64, 128, 90, 3.0),        # large scores: exercises the deferred rescale
+    (1200, 4, 1, 64, 100, 150, 1.0),      # segments with ragged shards (partial key tiles in the summary)
     (384, 1, 1, 128, 384, None, 1.0),     # one shard (plain blockwise attention)
 ]
 
@@ -158,6 +159,14 @@ def test_config_sampled_rows(cfg):
     w = WORKLOADS[cfg]
     x, out, lse = sampled_check(w)
     closed_form_checks(w, x, out, lse)
+
+
+def test_packed_documents_with_more_key_tiles_than_the_segment_summary():
+    """D = 64 with 9 x 32 shards x 16 tiles = 4,608 key tiles, more than the 4,096 entries of the
+    kernel's shared-memory segment summary: the producer then reads each tile's ids itself."""
+    w = Workload("packed documents B9 S65536 H1 D64, 32 shards", 9, 65536, 1, 64, "bf16", 1, 32, 2048, 2048,
+                 scale=0.5, segments=True, seed=4242)
+    sampled_check(w, nrows=2048)
 
 
 @pytest.mark.slow
