@@ -129,6 +129,16 @@ struct BwdParams {
   int vlog_cap;
 };
 
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {  // non-suspending test
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ void red_add_v2(float* addr, float a, float b) {
   asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "f"(a), "f"(b) : "memory");
 }
@@ -509,7 +519,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int next_kind = kRecStop;
         if (!fetch_kind(next_kind)) break;
         // wait for P^T, dS^T (TMEM) and dS^T (smem)
-        if (!mbar_wait(bars.pready(), pready_ph, ctl, 54)) break;
+        {  // spin (no suspend) for up to 4096 polls, then the bounded wait
+          bool got = false;
+          for (int n = 0; n < 4096 && !got; ++n) got = mbar_poll(bars.pready(), pready_ph);
+          if (!got && !mbar_wait(bars.pready(), pready_ph, ctl, 54)) break;
+        }
         pready_ph ^= 1;
         // the previous unit's dK / dV must have been read out before they are overwritten
         if (first && unit_n > 0 && !mbar_wait(bars.accfree(), (unit_n - 1) & 1, ctl, 55)) break;
